@@ -1,0 +1,393 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one attn_fwd call (the whole path: tensor maps, the prefill
+kernel, or the split-KV decode kernel plus its combine kernel) over one batch
+of synthetic bf16 inputs already resident in HBM.  L2 is flushed (a 256 MB
+write) before every step, outside the per-step CUDA events; the timed value is
+the sum of the per-step event durations on the launching stream, between a
+barrier + synchronize on both sides.  Multi-GPU runs (torchrun) are
+independent replicas of the same problem on each GPU ("weak" scaling): the
+path has no exchange step, so there is no collective on the data path.
+
+Rank 0 prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle
+(the only reference this path has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from blackwell_programming_gb300 import synthetic as syn  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (bf16, 1 GB300) and % of dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "gqa_causal_d128"
+L2_FLUSH_BYTES = 256 << 20
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {"prefill": "blackwell_programming_gb300/csrc/prefill_sm103.cu",
+                  "decode": "blackwell_programming_gb300/csrc/decode_sm103.cu"}
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Maximum of a float over all ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(units_per_rank: float, seconds_max: float, world: int) -> float:
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
+def load_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_hash(kind: str) -> str:
+    with open(os.path.join(ROOT, KERNEL_SOURCES[kind]), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel") != kind or e.get("source_sha256_16") != kernel_hash(kind):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "", 1).isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(wl, budget_s: float = 12.0):
+    """Time the fp64 oracle on whole (b, h) heads of the workload, bounded in time.
+
+    Returns (TFLOP/s, sample description, threads).  FLOPs of a head use the
+    reported formula (4*Nq*Nkv*d, halved when causal; 2*Nq*Nkv*(d_qk+d_v)).
+    """
+    import numpy as np
+    from oracle import attention_head
+    cores = blas_threads()
+    small = wl
+    # the decode shape has one query per head; take whole batch rows at a time
+    per_head = 2.0 * wl.Nq * wl.Nkv * (wl.d_qk + wl.d_v) / (2.0 if wl.causal else 1.0)
+    done, flops, t0 = 0, 0.0, time.perf_counter()
+    rng_heads = [(b, h) for b in range(small.B) for h in range(small.Hq)]
+    one = syn.Workload(wl.name + "_head", 1, 1, 1, wl.Nq, wl.Nkv, wl.d_qk, wl.d_v, wl.causal, wl.scale,
+                       wl.q_factor, wl.kv_factor, wl.v_aliases_k, wl.seed)
+    inp = syn.make_inputs(one)      # one head of the same distribution
+    q, k, v = inp.f64()
+    elapsed = 0.0
+    while done < len(rng_heads):
+        s = time.perf_counter()
+        attention_head(q[0, 0], k[0, 0], v[0, 0], wl.causal, wl.scale)
+        elapsed += time.perf_counter() - s
+        done += 1
+        flops += per_head
+        if elapsed >= budget_s or time.perf_counter() - t0 > 2 * budget_s:
+            break
+    desc = "%d of %d (batch, head) pairs of %s, full rows, fp64 numpy" % (done, len(rng_heads), wl.name)
+    return flops / elapsed / 1e12, desc, cores
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ main
+
+def run_reference(args, wl):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    t0 = time.time()
+    tflops = []
+    desc, cores = "", 1
+    for _ in range(args.warmup):
+        oracle_sample(wl, budget_s=1.0)
+    for _ in range(args.steps):
+        v, desc, cores = oracle_sample(wl, budget_s=args.ref_budget)
+        tflops.append(v)
+    value = statistics.median(tflops)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.time() - t0, 1)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl):
+    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "Nq": wl.Nq, "Nkv": wl.Nkv,
+            "d_qk": wl.d_qk, "d_v": wl.d_v, "causal": wl.causal, "scale": wl.scale,
+            "inputs": "seeded N(0,1) bf16 (q x%g, k/v x%g)" % (wl.q_factor, wl.kv_factor),
+            "l2": "flushed (256 MB write) before every step, outside the step events",
+            "parallelism": "replicas"}
+
+
+def measure_device(wl, steps, warmup, world, stream, flush, inputs):
+    """Per-step event times (seconds) of attn_fwd with resident inputs."""
+    import torch
+    import blackwell_programming_gb300 as gb
+    q, k, v = inputs
+    o = torch.empty((wl.B, wl.Hq, wl.Nq, wl.d_v), dtype=torch.float32, device="cuda")
+    lse = torch.empty((wl.B, wl.Hq, wl.Nq), dtype=torch.float32, device="cuda")
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.fill_(1.0)
+            gb.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse, stream=stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        for s, e in ev:
+            flush.fill_(1.0)
+            s.record(stream)
+            gb.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse, stream=stream)
+            e.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    assert gb.attn_check_device(stream) == 0, "kernel reported a timed-out wait"
+    return [s.elapsed_time(e) / 1e3 for s, e in ev]
+
+
+def measure_e2e(wl, steps, warmup, stream, host):
+    """Same metric with pinned host buffers: H2D inputs, attn_fwd, D2H O and LSE, per step."""
+    import torch
+    import blackwell_programming_gb300 as gb
+    hq, hk, hv = host
+    dq = torch.empty_like(hq, device="cuda")
+    dk = torch.empty_like(hk, device="cuda")
+    dv = torch.empty_like(hv, device="cuda") if hv is not None else None
+    ho = torch.empty((wl.B, wl.Hq, wl.Nq, wl.d_v), dtype=torch.float32).pin_memory()
+    hl = torch.empty((wl.B, wl.Hq, wl.Nq), dtype=torch.float32).pin_memory()
+    o = torch.empty_like(ho, device="cuda")
+    lse = torch.empty_like(hl, device="cuda")
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        if dv is not None:
+            dv.copy_(hv, non_blocking=True)
+        v = dv if dv is not None else dk[..., : wl.d_v]
+        gb.attn_fwd(dq, dk, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(steps):
+            step()
+        e.record(stream)
+        torch.cuda.synchronize()
+    secs = s.elapsed_time(e) / 1e3
+    h2d = hq.numel() * 2 + hk.numel() * 2 + (hv.numel() * 2 if hv is not None else 0)
+    d2h = ho.numel() * 4 + hl.numel() * 4
+    return secs, h2d, d2h
+
+
+def run_ours(args, wl):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    import blackwell_programming_gb300 as gb
+    gb.build()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, cores = oracle_sample(wl, budget_s=args.ref_budget)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    inp = syn.make_inputs(wl)
+    import numpy as np
+    hq = torch.from_numpy(inp.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(inp.k.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = None if inp.v is None else torch.from_numpy(inp.v.view(np.int16)).view(torch.bfloat16).pin_memory()
+    q, k = hq.cuda(), hk.cuda()
+    v = k[..., : wl.d_v] if hv is None else hv.cuda()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    clocks = ClockSampler(int(vis[local]) if local < len(vis) and vis[local].strip().isdigit() else local)
+    clocks.start()
+    times = measure_device(wl, args.steps, args.warmup, world, stream, flush, (q, k, v))
+    clk = clocks.stop()
+    total = sum(times)
+    t_max = reduce_max(total, world)
+    flops = wl.flops
+    value = aggregate(flops * args.steps, t_max, world) / 1e12
+
+    e2e_secs, h2d, d2h = measure_e2e(wl, args.steps, args.warmup, stream, (hq, hk, hv))
+    e2e_max = reduce_max(e2e_secs, world)
+    e2e_value = aggregate(flops * args.steps, e2e_max, world) / 1e12
+
+    peaks, peak_src = load_peaks()
+    kind = "decode" if wl.d_qk == 576 else "prefill"
+    per_launch = total / args.steps
+    if kind == "prefill":
+        achieved = flops / per_launch / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "peak_source": peak_src + " bf16_tflops (burst)",
+                "kernel": "prefill_kernel<128>" if wl.d_qk == 128 else "prefill_kernel<64>",
+                "algorithmic_flops_per_launch": flops}
+    else:
+        achieved = wl.algorithmic_bytes / per_launch / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_src + " hbm_gbs",
+                "kernel": "decode_kernel + combine_kernel (one step)",
+                "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
+                "tensor_tflops": flops / per_launch / 1e12}
+    roof["traffic"] = committed_traffic(kind, wl.name)
+    launches = (1 if kind == "prefill" else 2) * args.steps
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": workload_config(wl), "roofline": roof, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h},
+                "gpu_launches": launches, "clocks": clk,
+                "step_ms": {"min": min(times) * 1e3, "median": statistics.median(times) * 1e3,
+                            "max": max(times) * 1e3}}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)      # at least three untimed warm-up steps
+    wl = syn.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,160 @@
+"""Python binding of the C ABI in include/gbattn.h (ctypes, argument marshalling only).
+
+Every entry point here has the name of the C function it calls.  Torch is used
+for device memory and streams; all arithmetic runs in the library's kernels.
+There is no fallback: if libgbattn.so is missing or cannot be loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import _build
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_ERR_NO_DEVICE = 5
+
+# Symbols the shared library exports (the declarations of include/gbattn.h).
+EXPORTS = ("attn_fwd", "attn_check_device", "attn_status_string", "attn_last_cuda_error",
+           "attn_version", "attn_decode_workspace_bytes")
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(what)
+
+
+def load_library(path: str | None = None):
+    """Load libgbattn.so (built in-tree by ``_build.build``) and declare its ABI."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError("libgbattn.so is not built (expected at %s); call "
+                           "blackwell_programming_gb300.build() first" % path)
+    L = ctypes.CDLL(path)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
+    L.attn_fwd.restype = i
+    L.attn_check_device.argtypes = [vp, i]
+    L.attn_check_device.restype = i
+    L.attn_status_string.argtypes = [i]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_last_cuda_error.argtypes = []
+    L.attn_last_cuda_error.restype = ctypes.c_char_p
+    L.attn_version.argtypes = []
+    L.attn_version.restype = i
+    L.attn_decode_workspace_bytes.argtypes = [i, i, i]
+    L.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+    if path == _build.LIB:
+        _lib = L
+    return L
+
+
+def _raise(L, status: int, what: str):
+    msg = "%s: %s" % (what, L.attn_status_string(status).decode())
+    extra = L.attn_last_cuda_error().decode()
+    if extra:
+        msg += " (" + extra + ")"
+    raise AttnError(status, msg)
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(status).decode()
+
+
+def attn_version() -> int:
+    return load_library().attn_version()
+
+
+def attn_decode_workspace_bytes(B: int, Hkv: int, Nkv: int) -> int:
+    return load_library().attn_decode_workspace_bytes(B, Hkv, Nkv)
+
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def attn_check_device(stream=None, reset: bool = False, device=None) -> int:
+    """Synchronise the stream and read the kernels' error word (0 = ok)."""
+    L = load_library()
+    return L.attn_check_device(_stream_handle(stream, device), 1 if reset else 0)
+
+
+def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, Hq: int, Hkv: int,
+                 Nq: int, Nkv: int, d_qk: int, d_v: int, causal: bool, scale: float, stream_ptr: int = 0) -> int:
+    """The C call with raw integer pointers; returns the status code."""
+    L = load_library()
+    return L.attn_fwd(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
+                      ctypes.c_void_p(o_ptr), ctypes.c_void_p(lse_ptr), B, Hq, Hkv, Nq, Nkv, d_qk, d_v,
+                      1 if causal else 0, ctypes.c_float(scale), ctypes.c_void_p(stream_ptr))
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+             want_lse: bool = True, stream=None):
+    """O = softmax(mask(scale * Q K^T)) V and LSE on the GPU.
+
+    q: bf16 [B, Hq, Nq, d_qk]; k: bf16 [B, Hkv, Nkv, d_qk];
+    v: bf16 [B, Hkv, Nkv, d_v], or the view ``k[..., :d_v]`` of k (the latent
+    layout where V is the first d_v features of K).  All on one CUDA device,
+    contiguous (a view of k is accepted for v as described).  scale defaults
+    to 1/sqrt(d_qk).  Returns (o fp32 [B, Hq, Nq, d_v], lse fp32 [B, Hq, Nq]
+    or None).  Work is queued on ``stream`` (default: the current stream).
+    """
+    import torch
+    L = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("%s must be a torch.Tensor" % name)
+        if t.dtype != torch.bfloat16:
+            raise TypeError("%s must be bfloat16, got %s" % (name, t.dtype))
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+        if t.dim() != 4:
+            raise ValueError("%s must be 4-D [B, H, N, d]" % name)
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
+    B, Hq, Nq, d_qk = q.shape
+    Bk, Hkv, Nkv, dk = k.shape
+    Bv, Hv, Nv, d_v = v.shape
+    if Bk != B or Bv != B or Hv != Hkv or Nv != Nkv or dk != d_qk:
+        raise ValueError("shape mismatch: q %s k %s v %s" % (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
+    if not q.is_contiguous() or not k.is_contiguous():
+        raise ValueError("q and k must be contiguous [B, H, N, d] row-major tensors")
+    aliased = (v.data_ptr() == k.data_ptr() and d_v < d_qk and v.stride() == k.stride())
+    if not aliased and not v.is_contiguous():
+        raise ValueError("v must be contiguous, or the view k[..., :d_v]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_qk)
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, Hq, Nq, d_v), dtype=torch.float32, device=dev)
+    elif out.shape != (B, Hq, Nq, d_v) or out.dtype != torch.float32 or not out.is_contiguous() or out.device != dev:
+        raise ValueError("out must be a contiguous fp32 [B, Hq, Nq, d_v] tensor on q's device")
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    elif lse is not None and (lse.shape != (B, Hq, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [B, Hq, Nq] tensor")
+    v_ptr = k.data_ptr() if aliased else v.data_ptr()
+    with torch.cuda.device(dev):
+        st = L.attn_fwd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v_ptr),
+                        ctypes.c_void_p(out.data_ptr()),
+                        ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
+                        B, Hq, Hkv, Nq, Nkv, d_qk, d_v, 1 if causal else 0, ctypes.c_float(scale),
+                        _stream_handle(stream, dev))
+    if st != ATTN_OK:
+        _raise(L, st, "attn_fwd")
+    return out, lse

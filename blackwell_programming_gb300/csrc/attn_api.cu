@@ -1,0 +1,265 @@
+// attn_api.cu - the C ABI declared in include/gbattn.h: argument checks,
+// tensor-map (TMA descriptor) encoding, dispatch to the prefill or the
+// split-KV decode kernels, and the device error word.
+//
+// Tensor maps follow the "gl" global-layout idea of "Distilling a 4.5 hour
+// CUDA talk", section 10 (a shape-annotated pointer from which the copy
+// engine's descriptor is derived, with the swizzle chosen from the tile
+// width): every [B, H, N, d] tensor is described as a 3-D box grid
+// (d, N, B*H) with 64-feature (128-byte) boxes and the 128-byte swizzle, so a
+// tile that runs past N reads zeros instead of the next head's rows.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/gbattn.h"
+#include "internal.h"
+
+namespace gbattn {
+
+__device__ unsigned g_device_error = 0u;
+
+namespace {
+
+constexpr int kVersion = 100;
+constexpr int kMaxDevices = 64;
+
+thread_local char t_cuda_error[256] = "";
+
+int cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(t_cuda_error, sizeof(t_cuda_error), "%s: %s", where, cudaGetErrorString(e));
+  return ATTN_ERR_CUDA;
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  int status = ATTN_OK;
+  int num_sms = 0;
+  unsigned* err = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3) {
+      std::snprintf(t_cuda_error, sizeof(t_cuda_error), "device %d is sm_%d%d; this library is built for sm_103a",
+                    dev, major, minor);
+      return ATTN_ERR_NO_DEVICE;
+    }
+    if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_device_error)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    d.err = static_cast<unsigned*>(p);
+    if (g_encode == nullptr) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return cuda_fail(e == cudaSuccess ? cudaErrorNotSupported : e, "cuTensorMapEncodeTiled lookup");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return ATTN_OK;
+}
+
+// 3-D bf16 tensor map (inner features, rows, planes) with a 64 x box_rows x 1
+// box and the 128-byte swizzle.
+int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t planes,
+             uint64_t row_stride_bytes, uint64_t plane_stride_bytes, uint32_t box_rows) {
+  cuuint64_t dims[3] = {inner, rows, planes};
+  cuuint64_t strides[2] = {row_stride_bytes, plane_stride_bytes};
+  cuuint32_t box[3] = {64u, box_rows, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(t_cuda_error, sizeof(t_cuda_error), "cuTensorMapEncodeTiled failed (CUresult %d)",
+                  static_cast<int>(r));
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool check_env() {
+  static const bool on = [] {
+    const char* s = std::getenv("ATTN_CHECK");
+    return s != nullptr && s[0] == '1';
+  }();
+  return on;
+}
+
+int read_device_error(cudaStream_t stream, unsigned* err, int reset) {
+  unsigned h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, err, sizeof(h), cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(error word)");
+  if (reset) {
+    if ((e = cudaMemsetAsync(err, 0, sizeof(unsigned), stream)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemsetAsync(error word)");
+  }
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  return h ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+}  // namespace
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" {
+
+int attn_version(void) { return kVersion; }
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported shape";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "kernel wait timed out";
+    case ATTN_ERR_NO_DEVICE: return "no sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+const char* attn_last_cuda_error(void) { return t_cuda_error; }
+
+size_t attn_decode_workspace_bytes(int B, int Hkv, int Nkv) {
+  if (B <= 0 || Hkv <= 0 || Nkv <= 0) return 0;
+  DeviceInfo* d = nullptr;
+  if (device_info(&d) != ATTN_OK) return 0;
+  const int planes = B * Hkv;
+  const int tiles = decode_tiles(Nkv);
+  const long long total = 2LL * planes * tiles;
+  const int grid = static_cast<int>(std::min<long long>(total, d->num_sms));
+  const int ms = decode_max_segments(planes, tiles, grid);
+  return static_cast<size_t>(grid) * ms * 128 * (256 + 1) * sizeof(float);
+}
+
+int attn_check_device(attn_stream_t stream, int reset) {
+  DeviceInfo* d = nullptr;
+  int st = device_info(&d);
+  if (st != ATTN_OK) return st;
+  return read_device_error(reinterpret_cast<cudaStream_t>(stream), d->err, reset);
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq, int Hkv, int Nq,
+             int Nkv, int d_qk, int d_v, int causal, float scale, attn_stream_t stream_) {
+  t_cuda_error[0] = '\0';
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // ---------------------------------------------------------------- checks
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nkv <= 0 || d_qk <= 0 || d_v <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  const bool v_aliases_k = (v == k) && (d_v < d_qk);
+  if (v == k && d_v > d_qk) return ATTN_ERR_INVALID_ARG;
+  // sizes must fit the kernels' 32-bit row indexing
+  if (static_cast<long long>(B) * Hq * Nq >= (1LL << 31) || static_cast<long long>(B) * Hkv * Nkv >= (1LL << 31))
+    return ATTN_ERR_UNSUPPORTED;
+
+  const bool prefill = (d_qk == d_v) && (d_qk == 64 || d_qk == 128);
+  const bool decode = (d_qk == 576 && d_v == 512);
+  if (!prefill && !decode) return ATTN_ERR_UNSUPPORTED;
+  if (decode) {
+    // One query per sequence: with the bottom-right causal alignment it sees
+    // every key, so the causal flag changes nothing.
+    if (Nq != 1 || !v_aliases_k || Hq / Hkv > 128) return ATTN_ERR_UNSUPPORTED;
+  }
+
+  DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+
+  const float scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t e;
+
+  if (prefill) {
+    const int d = d_qk;
+    CUtensorMap tq, tk, tv;
+    const uint64_t rs = static_cast<uint64_t>(d) * 2;
+    if ((st = make_map(&tq, q, d, Nq, static_cast<uint64_t>(B) * Hq, rs, rs * Nq, 128)) != ATTN_OK) return st;
+    if ((st = make_map(&tk, k, d, Nkv, static_cast<uint64_t>(B) * Hkv, rs, rs * Nkv, 128)) != ATTN_OK) return st;
+    if ((st = make_map(&tv, v, d, Nkv, static_cast<uint64_t>(B) * Hkv, rs, rs * Nkv, 128)) != ATTN_OK) return st;
+    PrefillParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Nq = Nq;
+    p.Nkv = Nkv;
+    p.d_v = d_v;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale_log2;
+    p.nqb = (Nq + 255) / 256;
+    p.nkv_tiles = (Nkv + 127) / 128;
+    p.num_units = B * Hq * p.nqb;
+    p.err = dev->err;
+    if ((e = launch_prefill(d, tq, tk, tv, p, dev->num_sms, stream)) != cudaSuccess)
+      return cuda_fail(e, "prefill launch");
+  } else {
+    const int group = Hq / Hkv;
+    const int planes = B * Hkv;
+    CUtensorMap tq, tk;
+    const uint64_t rs = static_cast<uint64_t>(d_qk) * 2;
+    if ((st = make_map(&tq, q, d_qk, group, planes, rs, rs * group, 128)) != ATTN_OK) return st;
+    if ((st = make_map(&tk, k, d_qk, Nkv, planes, rs, rs * Nkv, 32)) != ATTN_OK) return st;
+    DecodeParams p{};
+    p.planes = planes;
+    p.group = group;
+    p.Nkv = Nkv;
+    p.tiles = decode_tiles(Nkv);
+    p.scale_log2 = scale_log2;
+    p.err = dev->err;
+    const long long total = 2LL * planes * p.tiles;
+    const int grid = static_cast<int>(std::min<long long>(total, dev->num_sms));
+    p.max_seg = decode_max_segments(planes, p.tiles, grid);
+    const size_t n_slots = static_cast<size_t>(grid) * p.max_seg * 128;
+    void* ws = nullptr;
+    if ((e = cudaMallocAsync(&ws, n_slots * (256 + 1) * sizeof(float), stream)) != cudaSuccess)
+      return cuda_fail(e, "cudaMallocAsync(decode workspace)");
+    p.o_part = static_cast<float*>(ws);
+    p.lse_part = p.o_part + n_slots * 256;
+    if ((e = launch_decode(tq, tk, p, grid, stream)) != cudaSuccess) {
+      cudaFreeAsync(ws, stream);
+      return cuda_fail(e, "decode launch");
+    }
+    if ((e = launch_combine(p, grid, o, lse, stream)) != cudaSuccess) {
+      cudaFreeAsync(ws, stream);
+      return cuda_fail(e, "combine launch");
+    }
+    if ((e = cudaFreeAsync(ws, stream)) != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(decode workspace)");
+  }
+
+  if (check_env()) return read_device_error(stream, dev->err, 0);
+  return ATTN_OK;
+}
+
+}  // extern "C"

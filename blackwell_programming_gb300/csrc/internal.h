@@ -1,0 +1,53 @@
+// internal.h - launch interfaces between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gbattn {
+
+// Prefill: one persistent CTA per SM walks "units" of two 128-row query
+// tiles of one (batch, head) pair.
+struct PrefillParams {
+  float* o;
+  float* lse;          // may be null
+  int B, Hq, Hkv, Nq, Nkv, d_v;
+  int causal;
+  float scale_log2;    // scale * log2(e)
+  int num_units;       // B * Hq * ceil(Nq / 256)
+  int nqb;             // ceil(Nq / 256)
+  int nkv_tiles;       // ceil(Nkv / 128)
+  unsigned* err;       // device error word
+};
+
+cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PrefillParams& p, int num_sms, cudaStream_t stream);
+
+// Split-KV decode for the latent head-dim 576 / 512 shape (V = first 512
+// features of K).  The Hq / Hkv query heads that share a KV head form the
+// rows of one 128-row tile; a "plane" is one (batch, KV head) pair.
+struct DecodeParams {
+  float* o_part;       // [grid * max_seg, 128, 256] partial O (normalised), per half
+  float* lse_part;     // [grid * max_seg, 128] partial LSE (natural log)
+  int planes;          // B * Hkv
+  int group;           // Hq / Hkv, <= 128
+  int Nkv;
+  int tiles;           // ceil(Nkv / 32)
+  int max_seg;         // partial slots per CTA
+  float scale_log2;    // scale * log2(e)
+  unsigned* err;
+};
+
+// Number of partial slots each CTA needs for a grid of `grid` CTAs.
+int decode_max_segments(int planes, int tiles, int grid);
+int decode_tiles(int Nkv);
+
+cudaError_t launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const DecodeParams& p, int grid,
+                          cudaStream_t stream);
+
+// Merge the partials of every row into O [planes * group, 512] and LSE.
+cudaError_t launch_combine(const DecodeParams& p, int grid, float* o, float* lse, cudaStream_t stream);
+
+}  // namespace gbattn

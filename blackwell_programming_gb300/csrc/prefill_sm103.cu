@@ -1,0 +1,454 @@
+// prefill_sm103.cu - fused attention forward (prefill), head dims 64 and 128.
+//
+// What it computes: O = softmax(mask(scale * Q K^T)) V and the row LSE,
+// streaming K/V tiles through the QK^T -> Mask -> Softmax -> x V pipeline of
+// "CS149 L11: Programming Specialized Hardware", section 5, with the online
+// softmax (running max and normaliser) of the FA2-style kernel in
+// "Distilling a 4.5 hour CUDA talk", section 7, and log2(e) folded into the
+// scale (same page, sections 2 and 7).
+//
+// How, on sm_103a (a design for this chip, not the pages' RTX 4090 / H100
+// kernels):
+//  * One persistent CTA per SM walks a static longest-first list of units; a
+//    unit is two 128-row query tiles (t = 0, 1) of one (batch, head).  The
+//    query heads that share a KV head are adjacent in the list so their K/V
+//    tiles are reused from L2 ("Distilling...", section 5, L2 super-blocks).
+//  * Warp 9 is the TMA producer: Q tiles once per unit, then a ring of K and
+//    a ring of V stages, each stage guarded by a full / empty mbarrier pair
+//    (expect-tx on full, tcgen05.commit on empty) - the producer/consumer
+//    template of "Distilling...", section 12, with the mbarrier handoff of
+//    section 13.
+//  * Warp 8 issues every tcgen05.mma from one thread.  S_t = Q_t K_j^T lands
+//    in tensor memory (TMEM); the softmax writes P_t (bf16) over S_t and the
+//    MMA computes O_t += P_t V_j with P read straight from TMEM.  The two
+//    query tiles ping-pong: the tensor core works on one tile while the
+//    softmax warpgroup of the other one runs.
+//  * Warpgroups 0 and 1 own query tile 0 and 1.  TMEM lane i is row i, so a
+//    thread owns a whole row: max, exp2 and sum stay in-thread.  They also
+//    rescale O (only when the running max grew by more than 2^8, which keeps
+//    the result exact) and run the epilogue: O / l and LSE to global memory.
+//
+// TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D).
+#include <cmath>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+constexpr int BM = 128;               // query rows per tile (TMEM lanes)
+constexpr int BN = 128;               // keys per K/V tile
+constexpr int kThreads = 384;         // 3 warpgroups
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only past 2^8
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+template <int D>
+struct Cfg {
+  static constexpr int KCH = D / 64;                 // 128-byte column chunks per row
+  static constexpr uint32_t Q_BYTES = BM * D * 2;
+  static constexpr uint32_t KV_BYTES = BN * D * 2;
+  static constexpr uint32_t CHUNK_Q = BM * 128;      // one 64-column chunk of a Q tile
+  static constexpr uint32_t CHUNK_KV = BN * 128;
+  static constexpr int KS = (D == 128) ? 3 : 4;      // K stages
+  static constexpr int VS = (D == 128) ? 2 : 4;      // V stages
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + VS * KV_BYTES;
+  // barrier indices
+  static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 4 + KS, B_VFULL = 4 + 2 * KS,
+                       B_VEMPTY = 4 + 2 * KS + VS, B_SFULL = 4 + 2 * KS + 2 * VS, B_PFULL = B_SFULL + 2,
+                       B_OFULL = B_PFULL + 2, B_OEMPTY = B_OFULL + 2, B_DRAIN = B_OEMPTY + 2,
+                       NUM_BARS = B_DRAIN + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alignment
+  // TMEM column of S_t and O_t
+  __device__ static constexpr uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
+  __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * D; }
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, false, true);
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+struct Unit {
+  int b, h, qb;
+  int n[2];   // K/V tiles visited by query tile 0 / 1
+};
+
+__device__ __forceinline__ int kv_tiles_for(int q0, const PrefillParams& p) {
+  if (q0 >= p.Nq) return 0;
+  if (!p.causal) return p.nkv_tiles;
+  const int last_row = min(q0 + BM - 1, p.Nq - 1);
+  const int last_key = last_row + (p.Nkv - p.Nq);
+  if (last_key < 0) return 0;
+  return min(last_key / BN + 1, p.nkv_tiles);
+}
+
+// Unit u: query-block index descending (longest causal work first), then
+// (batch, head) with the heads of one KV group adjacent.
+__device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p) {
+  Unit U;
+  const int bh_count = p.B * p.Hq;
+  const int qb_rev = u / bh_count;
+  const int bh = u - qb_rev * bh_count;
+  U.qb = p.nqb - 1 - qb_rev;
+  U.b = bh / p.Hq;
+  U.h = bh - U.b * p.Hq;
+  U.n[0] = kv_tiles_for(U.qb * 2 * BM, p);
+  U.n[1] = kv_tiles_for(U.qb * 2 * BM + BM, p);
+  return U;
+}
+
+// Snake order over rounds of gridDim.x units.
+__device__ __forceinline__ int unit_at(int it) {
+  const int base = it * static_cast<int>(gridDim.x);
+  return (it & 1) ? base + static_cast<int>(gridDim.x - 1 - blockIdx.x) : base + static_cast<int>(blockIdx.x);
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+  const bool ok = mbar_wait(bar, parity, w);
+  return __all_sync(kFull, ok);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+  auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::OFF_MISC + 4);
+  const WaitCtx wctx{abort_flag, p.err};
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::B_QFULL + t), 1);
+      mbar_init(bar(C::B_QEMPTY + t), 1);
+      mbar_init(bar(C::B_SFULL + t), 1);
+      mbar_init(bar(C::B_PFULL + t), 4);
+      mbar_init(bar(C::B_OFULL + t), 1);
+      mbar_init(bar(C::B_OEMPTY + t), 4);
+    }
+    for (int s = 0; s < C::KS; ++s) {
+      mbar_init(bar(C::B_KFULL + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::VS; ++s) {
+      mbar_init(bar(C::B_VFULL + s), 1);
+      mbar_init(bar(C::B_VEMPTY + s), 1);
+    }
+    mbar_init(bar(C::B_DRAIN), 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tmem_slot;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const uint64_t pol_q = l2_policy_evict_first();
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0, qph[2] = {0, 0};
+      int k_last[C::KS], v_last[C::VS];   // parity of the last fill of each stage, -1 = none
+      int q_last[2] = {-1, -1};
+      for (int s = 0; s < C::KS; ++s) k_last[s] = -1;
+      for (int s = 0; s < C::VS; ++s) v_last[s] = -1;
+      const int group = p.Hq / p.Hkv;
+      for (int it = 0;; ++it) {
+        const int u = unit_at(it);
+        if (u >= p.num_units) break;
+        const Unit U = decode_unit(u, p);
+        bool ok = true;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (U.n[t] == 0) continue;
+          if (!(ok = mbar_wait(bar(C::B_QEMPTY + t), qph[t] ^ 1u, wctx))) break;
+          qph[t] ^= 1u;
+          mbar_arrive_expect_tx(bar(C::B_QFULL + t), C::Q_BYTES);
+          q_last[t] = static_cast<int>(qph[t] ^ 1u);
+          for (int kc = 0; kc < C::KCH; ++kc)
+            tma_load_3d(sQ + t * C::Q_BYTES + kc * C::CHUNK_Q, &tmQ, bar(C::B_QFULL + t), kc * 64,
+                        (U.qb * 2 + t) * BM, U.b * p.Hq + U.h, pol_q);
+        }
+        if (!ok) break;
+        const int nmax = max(U.n[0], U.n[1]);
+        const int z = U.b * p.Hkv + U.h / group;
+        for (int j = 0; j < nmax && ok; ++j) {
+          if (!(ok = mbar_wait(bar(C::B_KEMPTY + ks), kph ^ 1u, wctx))) break;
+          mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::KV_BYTES);
+          k_last[ks] = static_cast<int>(kph);
+          for (int kc = 0; kc < C::KCH; ++kc)
+            tma_load_3d(sK + ks * C::KV_BYTES + kc * C::CHUNK_KV, &tmK, bar(C::B_KFULL + ks), kc * 64, j * BN,
+                        z, pol_kv);
+          if (++ks == C::KS) { ks = 0; kph ^= 1u; }
+          if (!(ok = mbar_wait(bar(C::B_VEMPTY + vs), vph ^ 1u, wctx))) break;
+          mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::KV_BYTES);
+          v_last[vs] = static_cast<int>(vph);
+          for (int kc = 0; kc < C::KCH; ++kc)
+            tma_load_3d(sV + vs * C::KV_BYTES + kc * C::CHUNK_KV, &tmV, bar(C::B_VFULL + vs), kc * 64, j * BN,
+                        z, pol_kv);
+          if (++vs == C::VS) { vs = 0; vph ^= 1u; }
+        }
+        if (!ok) break;
+      }
+      // Every issued copy must have landed before the CTA may exit.
+      for (int t = 0; t < 2; ++t)
+        if (q_last[t] >= 0) mbar_wait_drain(bar(C::B_QFULL + t), static_cast<uint32_t>(q_last[t]));
+      for (int s = 0; s < C::KS; ++s)
+        if (k_last[s] >= 0) mbar_wait_drain(bar(C::B_KFULL + s), static_cast<uint32_t>(k_last[s]));
+      for (int s = 0; s < C::VS; ++s)
+        if (v_last[s] >= 0) mbar_wait_drain(bar(C::B_VFULL + s), static_cast<uint32_t>(v_last[s]));
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0, qph[2] = {0, 0}, pph[2] = {0, 0}, oeph[2] = {0, 0};
+      for (int it = 0;; ++it) {
+        const int u = unit_at(it);
+        if (u >= p.num_units) break;
+        const Unit U = decode_unit(u, p);
+        const int nmax = max(U.n[0], U.n[1]);
+        bool o_waited[2] = {false, false};
+        bool ok = true;
+        for (int j = 0; j <= nmax && ok; ++j) {
+          if (j < nmax) {
+            if (!(ok = mbar_wait(bar(C::B_KFULL + ks), kph, wctx))) break;
+          }
+          if (j >= 1) {
+            if (!(ok = mbar_wait(bar(C::B_VFULL + vs), vph, wctx))) break;
+          }
+          tc_fence_after();
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= 1 && j - 1 < U.n[t]) {
+              if (!o_waited[t]) {
+                if (!(ok = mbar_wait(bar(C::B_OEMPTY + t), oeph[t] ^ 1u, wctx))) break;
+                oeph[t] ^= 1u;
+                o_waited[t] = true;
+              }
+              if (!(ok = mbar_wait(bar(C::B_PFULL + t), pph[t], wctx))) break;
+              pph[t] ^= 1u;
+              tc_fence_after();
+              const uint32_t vbase = sV + vs * C::KV_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < BN / 16; ++kk) {
+                const uint64_t bdesc = smem_desc_sw128(vbase + kk * 16 * 128, C::CHUNK_KV, 1024);
+                mma_ts(tm + C::col_o(t), tm + C::col_s(t) + kk * 8, bdesc, C::IDESC_PV,
+                       (j - 1 > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            if (j < U.n[t]) {
+              if (j == 0) {
+                if (!(ok = mbar_wait(bar(C::B_QFULL + t), qph[t], wctx))) break;
+                qph[t] ^= 1u;
+                tc_fence_after();
+              }
+              const uint32_t qbase = sQ + t * C::Q_BYTES;
+              const uint32_t kbase = sK + ks * C::KV_BYTES;
+#pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off_q = (kk >> 2) * C::CHUNK_Q + (kk & 3) * 32;
+                const uint32_t off_k = (kk >> 2) * C::CHUNK_KV + (kk & 3) * 32;
+                mma_ss(tm + C::col_s(t), smem_desc_sw128(qbase + off_q, 16, 1024),
+                       smem_desc_sw128(kbase + off_k, 16, 1024), C::IDESC_S, kk > 0 ? 1u : 0u);
+              }
+              mma_commit(bar(C::B_SFULL + t));
+              if (j == U.n[t] - 1) mma_commit(bar(C::B_QEMPTY + t));
+            } else if (j == U.n[t] && U.n[t] > 0) {
+              mma_commit(bar(C::B_OFULL + t));
+            }
+          }
+          if (!ok) break;
+          if (j < nmax) {
+            mma_commit(bar(C::B_KEMPTY + ks));
+            if (++ks == C::KS) { ks = 0; kph ^= 1u; }
+          }
+          if (j >= 1) {
+            mma_commit(bar(C::B_VEMPTY + vs));
+            if (++vs == C::VS) { vs = 0; vph ^= 1u; }
+          }
+        }
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!o_waited[t]) {
+            if (!(ok = mbar_wait(bar(C::B_OEMPTY + t), oeph[t] ^ 1u, wctx))) break;
+            oeph[t] ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+      // Let every issued MMA finish before TMEM is released.
+      mma_commit(bar(C::B_DRAIN));
+      mbar_wait_drain(bar(C::B_DRAIN), 0);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------ softmax + epilogue
+    const int t = static_cast<int>(warp >> 2);
+    const uint32_t quad = warp & 3u;
+    const int row_in_tile = static_cast<int>(quad * 32 + lane);
+    const uint32_t lane_addr = (quad * 32u) << 16;
+    const uint32_t tS = tm + lane_addr + C::col_s(t);
+    const uint32_t tO = tm + lane_addr + C::col_o(t);
+    const float sl2 = p.scale_log2;
+    const int delta = p.Nkv - p.Nq;
+    uint32_t sph = 0, ofph = 0;
+    for (int it = 0;; ++it) {
+      const int u = unit_at(it);
+      if (u >= p.num_units) break;
+      const Unit U = decode_unit(u, p);
+      const int n = U.n[t];
+      const int q0 = (U.qb * 2 + t) * BM;
+      const int row = q0 + row_in_tile;
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        if (!(ok = warp_wait(bar(C::B_SFULL + t), sph, wctx))) break;
+        sph ^= 1u;
+        tc_fence_after();
+        const int key0 = j * BN;
+        const bool need_mask = (key0 + BN > p.Nkv) || (p.causal && key0 + BN - 1 > q0 + delta);
+        const int key_lim = p.causal ? min(row + delta, p.Nkv - 1) : p.Nkv - 1;   // last visible key
+        // pass 1: row maximum of the raw logits
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tS + c * 32, v);
+          if (need_mask) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (key0 + c * 32 + i > key_lim) v[i] = -INFINITY;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
+        }
+        const float m_new = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+        float alpha = 1.f;
+        const bool grow = m_new > m_used + kRescaleThreshold;
+        if (grow) {
+          alpha = ex2(m_used - m_new);
+          m_used = m_new;
+        }
+        l *= alpha;
+        if (j > 0 && __any_sync(kFull, grow)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tO + c * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+        const float base = (m_used == -INFINITY) ? 0.f : m_used;
+        // pass 2: P = 2^(s * scale * log2 e - m), row sum, P as bf16 over S
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          tmem_ld32(tS + c * 32, v);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float p0 = ex2(fmaf(v[2 * i], sl2, -base));
+            float p1 = ex2(fmaf(v[2 * i + 1], sl2, -base));
+            if (need_mask) {
+              if (key0 + c * 32 + 2 * i > key_lim) p0 = 0.f;
+              if (key0 + c * 32 + 2 * i + 1 > key_lim) p1 = 0.f;
+            }
+            l += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + c * 16, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_PFULL + t));
+      }
+      if (!ok) break;
+      // epilogue: O / l and LSE, then hand O_t back to the MMA warp
+      if (n > 0) {
+        if (!(ok = warp_wait(bar(C::B_OFULL + t), ofph, wctx))) break;
+        ofph ^= 1u;
+        tc_fence_after();
+      }
+      const bool live = row < p.Nq;
+      float* orow = p.o + (static_cast<size_t>(U.b * p.Hq + U.h) * p.Nq + (live ? row : 0)) * D;
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float v[32];
+        if (n > 0) {
+          tmem_ld32(tO + c * 32, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        if (live) {
+          float4* dst = reinterpret_cast<float4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(v[4 * i] * inv_l, v[4 * i + 1] * inv_l, v[4 * i + 2] * inv_l, v[4 * i + 3] * inv_l);
+        }
+      }
+      if (live && p.lse != nullptr) {
+        const float lse = (l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        p.lse[static_cast<size_t>(U.b * p.Hq + U.h) * p.Nq + row] = lse;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + t));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tm, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                     int num_sms, cudaStream_t stream) {
+  using C = Cfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  const int grid = min(p.num_units, num_sms);
+  if (grid <= 0) return cudaSuccess;
+  prefill_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PrefillParams& p, int num_sms, cudaStream_t stream) {
+  if (d == 64) return launch_d<64>(tq, tk, tv, p, num_sms, stream);
+  if (d == 128) return launch_d<128>(tq, tk, tv, p, num_sms, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gbattn

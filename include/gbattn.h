@@ -1,0 +1,114 @@
+/*
+ * gbattn.h - fused attention forward for one NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * The operation is the FlashAttention forward
+ *
+ *     O = softmax(mask(scale * Q K^T)) V,     LSE_i = log sum_j exp(scale * q_i . k_j)
+ *
+ * computed tile by tile without materialising the score matrix.  Its stage
+ * order (QK^T -> Mask -> Softmax -> x V) is the FlashAttention metapipeline of
+ * "CS149 L11: Programming Specialized Hardware", section 5; the softmax is the
+ * Map(exp) / Reduce(+) / Zip(/) chain of the same section, evaluated online
+ * with a running row maximum and normaliser as in the FA2-style kernel of
+ * "Distilling a 4.5 hour CUDA talk", section 7, with log2(e) folded into the
+ * scale (sections 2 and 7 of that page).
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device; the
+ *    caller owns every buffer.  Nothing is freed or retained after return.
+ *  - Layouts are dense row-major [batch, head, sequence, feature], the
+ *    {batch, head, seq, col} four-dimensional global layout of "Distilling a
+ *    4.5 hour CUDA talk", sections 7 and 10.
+ *  - Work is enqueued on `stream` (NULL = the legacy default stream) and the
+ *    call returns without waiting for it.  The caller synchronises.
+ *  - Errors are returned as attn_status codes; nothing prints, throws or exits.
+ *  - Host threads may call concurrently on different streams; the library
+ *    keeps no mutable device state across calls except the device error word
+ *    read by attn_check_device().
+ */
+#ifndef GBATTN_H
+#define GBATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, spelled without the CUDA headers. */
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, Hq % Hkv != 0,
+                                  misaligned pointer, bad scale, bad aliasing   */
+    ATTN_ERR_UNSUPPORTED = 2,  /* head dims not built, or causal decode shape   */
+    ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed             */
+    ATTN_ERR_TIMEOUT = 4,      /* a kernel gave up on a bounded wait            */
+    ATTN_ERR_NO_DEVICE = 5     /* no sm_103 device is current                   */
+} attn_status;
+
+/*
+ * attn_fwd - attention forward, O and LSE.
+ *
+ *  q    bf16 [B, Hq,  Nq,  d_qk], contiguous.
+ *  k    bf16 [B, Hkv, Nkv, d_qk], contiguous.
+ *  v    bf16 [B, Hkv, Nkv, d_v], contiguous; OR v == k with d_v < d_qk, in
+ *       which case V is the first d_v features of each K row (row stride d_qk),
+ *       the head-dim 576/512 latent layout of "Distilling a 4.5 hour CUDA
+ *       talk", sections 12-13.
+ *  o    fp32 [B, Hq, Nq, d_v], written.
+ *  lse  fp32 [B, Hq, Nq], written: natural-log log-sum-exp of the scaled
+ *       logits over the visible keys; -inf for a row with no visible key (its
+ *       O row is 0).  May be NULL to skip it.
+ *  Hq % Hkv == 0; query head h reads KV head h / (Hq / Hkv).
+ *  causal != 0: key j is visible to query i iff j <= i + (Nkv - Nq)
+ *       (aligned at the bottom-right corner; the plain lower triangle when
+ *       Nq == Nkv).
+ *  scale >= 0 and finite; the logits are scale * q_i . k_j.
+ *
+ * Supported (d_qk, d_v): (64, 64) and (128, 128) through the prefill kernel,
+ * any Nq and Nkv >= 1; (576, 512) with Nq == 1, non-causal, through the
+ * split-KV decode kernel plus a combine kernel.  The decode path takes a
+ * stream-ordered workspace (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *
+ * Pointers must be 16-byte aligned (the tensor-memory-accelerator rule).
+ * Returns ATTN_OK once the kernels are enqueued.  Device-side failures are
+ * reported later by attn_check_device().  With the environment variable
+ * ATTN_CHECK=1 the call synchronises `stream` and reports them itself.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse,
+             int B, int Hq, int Hkv, int Nq, int Nkv, int d_qk, int d_v,
+             int causal, float scale, attn_stream_t stream);
+
+/*
+ * attn_check_device - synchronise `stream` and read the device error word
+ * that the kernels set when a bounded wait gives up (see
+ * ATTN_ERR_TIMEOUT).  reset != 0 clears the word.  Returns ATTN_OK,
+ * ATTN_ERR_TIMEOUT or ATTN_ERR_CUDA.
+ */
+int attn_check_device(attn_stream_t stream, int reset);
+
+/* attn_status_string - static text for a status code (never NULL). */
+const char* attn_status_string(int status);
+
+/* attn_last_cuda_error - static text of the last CUDA error seen by this
+ * thread's most recent failing call ("" if none). */
+const char* attn_last_cuda_error(void);
+
+/* attn_version - 100 * major + minor of this library. */
+int attn_version(void);
+
+/*
+ * attn_decode_workspace_bytes - bytes of stream-ordered workspace attn_fwd
+ * allocates (and frees, on the same stream) for a (576, 512) decode shape
+ * with B * Hkv KV planes and Nkv keys on the current device.  0 if the
+ * arguments are not positive or no sm_103 device is current.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hkv, int Nkv);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBATTN_H */

@@ -1,0 +1,96 @@
+"""The C-ABI library builds, loads and exports what include/gbattn.h declares.
+
+These run without a GPU: only calls that return before touching CUDA are made
+(argument checks), no compute.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import blackwell_programming_gb300 as gb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gbattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gb.build()
+    return gb.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    assert declared_functions() == sorted(gb.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_exported_symbols_via_nm(lib):
+    import shutil
+    import subprocess
+    if shutil.which("nm") is None:
+        pytest.skip("nm not available")
+    out = subprocess.run(["nm", "-D", "--defined-only", gb._build.LIB], capture_output=True, text=True).stdout
+    names = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in names, name
+
+
+def test_version_and_strings(lib):
+    assert gb.attn_version() == 100
+    assert gb.attn_status_string(gb.ATTN_OK) == "ok"
+    assert gb.attn_status_string(gb.ATTN_ERR_INVALID_ARG) == "invalid argument"
+    assert gb.attn_status_string(gb.ATTN_ERR_TIMEOUT) == "kernel wait timed out"
+    assert gb.attn_status_string(12345) == "unknown status"
+
+
+GOOD = dict(B=1, Hq=2, Hkv=1, Nq=128, Nkv=128, d_qk=128, d_v=128, causal=False, scale=0.1)
+P = 1 << 20   # a 16-byte-aligned fake address; never dereferenced because the checks fail first
+
+
+def call(**kw):
+    a = dict(GOOD)
+    ptrs = dict(q_ptr=P, k_ptr=P * 2, v_ptr=P * 3, o_ptr=P * 4, lse_ptr=P * 5)
+    for key in list(kw):
+        if key in ptrs:
+            ptrs[key] = kw.pop(key)
+    a.update(kw)
+    return gb.attn_fwd_raw(ptrs["q_ptr"], ptrs["k_ptr"], ptrs["v_ptr"], ptrs["o_ptr"], ptrs["lse_ptr"],
+                           a["B"], a["Hq"], a["Hkv"], a["Nq"], a["Nkv"], a["d_qk"], a["d_v"], a["causal"],
+                           a["scale"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(q_ptr=0), dict(k_ptr=0), dict(v_ptr=0), dict(o_ptr=0),
+    dict(B=0), dict(Hq=0), dict(Hkv=-1), dict(Nq=0), dict(Nkv=0), dict(d_qk=0), dict(d_v=0),
+    dict(Hq=3, Hkv=2),
+    dict(scale=float("nan")), dict(scale=float("inf")), dict(scale=-1.0),
+    dict(q_ptr=P + 8), dict(k_ptr=P + 2), dict(o_ptr=P + 4), dict(lse_ptr=P + 2),
+])
+def test_invalid_arguments_rejected_before_any_cuda_call(lib, bad):
+    assert call(**bad) == gb.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bad", [
+    dict(d_qk=96, d_v=96), dict(d_qk=128, d_v=64), dict(d_qk=256, d_v=256),
+    dict(d_qk=576, d_v=512, Nq=2),                        # latent shape: decode only
+    dict(d_qk=576, d_v=512, Nq=1),                        # latent shape needs v == k
+    dict(d_qk=576, d_v=512, Nq=1, Hq=256, Hkv=1, v_ptr=P * 2),   # > 128 heads per KV head
+])
+def test_unsupported_shapes(lib, bad):
+    assert call(**bad) == gb.ATTN_ERR_UNSUPPORTED
+
+
+def test_v_longer_than_k_alias_rejected(lib):
+    assert call(v_ptr=P * 2, d_qk=64, d_v=128) == gb.ATTN_ERR_INVALID_ARG

@@ -1,0 +1,173 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small problems (several tiles and a ragged tail) are compared element by
+element in full; the five workload shapes at full size are compared on
+sampled rows that the oracle evaluates one by one.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from blackwell_programming_gb300 import synthetic as syn
+from oracle import attention, attention_head, attention_rows
+from tests.parity_util import check, run_gpu, to_torch
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import blackwell_programming_gb300 as gb
+    gb.build()
+
+
+def full_case(wl):
+    inp = syn.make_inputs(wl)
+    o, lse = run_gpu(inp)
+    q, k, v = inp.f64()
+    o_ref, lse_ref = attention(q, k, v, wl.causal, wl.scale)
+    return check(o.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, wl.name)
+
+
+def W(name, **kw):
+    return syn.Workload(name, **kw)
+
+
+SMALL = [
+    W("one_tile_d64", B=1, Hq=1, Hkv=1, Nq=128, Nkv=128, d_qk=64, d_v=64, causal=False, scale=0.125),
+    W("ragged_d128_causal", B=1, Hq=2, Hkv=2, Nq=200, Nkv=200, d_qk=128, d_v=128, causal=True, scale=0.09),
+    W("ragged_d64_rect", B=2, Hq=2, Hkv=1, Nq=77, Nkv=300, d_qk=64, d_v=64, causal=False, scale=0.125),
+    W("causal_nq_gt_nkv", B=1, Hq=2, Hkv=1, Nq=300, Nkv=129, d_qk=128, d_v=128, causal=True, scale=0.088),
+    W("causal_nq_lt_nkv", B=1, Hq=3, Hkv=1, Nq=100, Nkv=333, d_qk=64, d_v=64, causal=True, scale=0.125),
+    W("single_query_d128", B=2, Hq=4, Hkv=2, Nq=1, Nkv=513, d_qk=128, d_v=128, causal=False, scale=0.088),
+    W("single_key_d64", B=1, Hq=1, Hkv=1, Nq=130, Nkv=1, d_qk=64, d_v=64, causal=False, scale=0.125),
+    W("gqa_multi_unit_d128", B=2, Hq=8, Hkv=2, Nq=640, Nkv=640, d_qk=128, d_v=128, causal=True, scale=0.088),
+    W("noncausal_many_tiles_d128", B=1, Hq=4, Hkv=4, Nq=384, Nkv=1000, d_qk=128, d_v=128, causal=False,
+      scale=0.088, q_factor=4.0),
+    W("zero_scale_d64", B=1, Hq=1, Hkv=1, Nq=256, Nkv=384, d_qk=64, d_v=64, causal=False, scale=0.0),
+    W("decode_small", B=2, Hq=16, Hkv=1, Nq=1, Nkv=300, d_qk=576, d_v=512, causal=False,
+      scale=1 / math.sqrt(192), v_aliases_k=True),
+    W("decode_two_kv_heads", B=3, Hq=64, Hkv=2, Nq=1, Nkv=1111, d_qk=576, d_v=512, causal=True,
+      scale=1 / math.sqrt(192), v_aliases_k=True),
+]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_small_full_parity(wl):
+    full_case(wl)
+
+
+def test_workload_tile_d64_full():
+    full_case(syn.WORKLOADS["tile_d64"])
+
+
+def test_workload_causal_d64_bigq_full():
+    full_case(syn.WORKLOADS["causal_d64_bigq"])
+
+
+def sampled_rows(n):
+    base = [0, 1, 127, 128, 129, 255, 256, n // 2, n - 129, n - 128, n - 2, n - 1]
+    r = np.random.default_rng(n)
+    return sorted({x for x in base + list(r.integers(0, n, 20)) if 0 <= x < n})
+
+
+@pytest.mark.parametrize("name", ["gqa_causal_d128", "long_causal_d128"])
+def test_workload_prefill_full_size_sampled(name):
+    wl = syn.WORKLOADS[name]
+    inp = syn.make_inputs(wl)
+    o, lse = run_gpu(inp)
+    o = o.cpu().numpy()
+    lse = lse.cpu().numpy()
+    q, k, v = inp.f64()
+    rows = sampled_rows(wl.Nq)
+    heads = [(0, 0), (0, 3), (0, 4), (wl.B - 1, wl.Hq - 1), (wl.B // 2, wl.Hq // 2 + 1)]
+    for b, h in heads:
+        o_ref, lse_ref = attention_rows(q, k, v, wl.causal, wl.scale, b, h, rows)
+        check(o[b, h, rows], lse[b, h, rows], o_ref, lse_ref, "%s b=%d h=%d" % (name, b, h))
+    # properties that hold at any size, on every row
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    # causal row 0 of every head attends only to key 0: O = V[0], LSE = s_00
+    kv = np.arange(wl.Hq) // (wl.Hq // wl.Hkv)
+    v0 = v[:, kv, 0, :]
+    assert np.max(np.abs(o[:, :, 0, :] - v0)) <= 1e-2
+
+
+def test_workload_decode_full_size_sampled():
+    wl = syn.WORKLOADS["decode_d576"]
+    inp = syn.make_inputs(wl)
+    o, lse = run_gpu(inp)
+    o = o.cpu().numpy()
+    lse = lse.cpu().numpy()
+    q, k, _ = inp.f64()
+    r = np.random.default_rng(5)
+    pairs = [(0, 0), (0, 127), (63, 0), (63, 127), (31, 64)] + [(int(b), int(h)) for b, h in
+                                                             zip(r.integers(0, 64, 40), r.integers(0, 128, 40))]
+    for b, h in pairs:
+        o_ref, lse_ref = attention_head(q[b, h], k[b, 0], k[b, 0, :, :512], False, wl.scale)
+        check(o[b, h], lse[b, h], o_ref, lse_ref, "decode b=%d h=%d" % (b, h))
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
+def test_deterministic_and_nondefault_stream():
+    wl = W("det", B=1, Hq=4, Hkv=2, Nq=384, Nkv=384, d_qk=128, d_v=128, causal=True, scale=0.088)
+    inp = syn.make_inputs(wl)
+    o1, l1 = run_gpu(inp)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o2, l2 = run_gpu(inp, stream=s)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_decode_deterministic():
+    wl = W("decdet", B=2, Hq=32, Hkv=1, Nq=1, Nkv=700, d_qk=576, d_v=512, causal=False,
+           scale=1 / math.sqrt(192), v_aliases_k=True)
+    inp = syn.make_inputs(wl)
+    o1, l1 = run_gpu(inp)
+    o2, l2 = run_gpu(inp)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_writes_stay_in_bounds(d, causal):
+    import blackwell_programming_gb300 as gb
+    wl = W("canary", B=1, Hq=2, Hkv=1, Nq=130, Nkv=200, d_qk=d, d_v=d, causal=causal, scale=0.1)
+    inp = syn.make_inputs(wl)
+    q, k, v = to_torch(inp)
+    n_o = 2 * 130 * d
+    pad = 4096
+    big_o = torch.full((n_o + 2 * pad,), 12345.0, device="cuda")
+    big_l = torch.full((2 * 130 + 2 * pad,), 12345.0, device="cuda")
+    st = gb.attn_fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), big_o[pad:].data_ptr(),
+                         big_l[pad:].data_ptr(), 1, 2, 1, 130, 200, d, d, causal, 0.1,
+                         torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.all(big_o[:pad] == 12345.0) and torch.all(big_o[pad + n_o:] == 12345.0)
+    assert torch.all(big_l[:pad] == 12345.0) and torch.all(big_l[pad + 260:] == 12345.0)
+    qf, kf, vf = inp.f64()
+    o_ref, lse_ref = attention(qf, kf, vf, causal, 0.1)
+    check(big_o[pad:pad + n_o].view(1, 2, 130, d).cpu().numpy(), big_l[pad:pad + 260].view(1, 2, 130).cpu().numpy(),
+          o_ref, lse_ref, "canary")
+
+
+def test_lse_optional():
+    import blackwell_programming_gb300 as gb
+    wl = W("nolse", B=1, Hq=1, Hkv=1, Nq=256, Nkv=256, d_qk=64, d_v=64, causal=True, scale=0.125)
+    inp = syn.make_inputs(wl)
+    q, k, v = to_torch(inp)
+    o, lse = gb.attn_fwd(q, k, v, causal=True, scale=0.125, want_lse=False)
+    torch.cuda.synchronize()
+    assert lse is None
+    qf, kf, vf = inp.f64()
+    o_ref, lse_ref = attention(qf, kf, vf, True, 0.125)
+    assert np.max(np.abs(o.cpu().numpy() - o_ref)) <= 2e-2
+
+
+def test_error_word_clear_after_runs():
+    import blackwell_programming_gb300 as gb
+    assert gb.attn_check_device(reset=True) == 0
