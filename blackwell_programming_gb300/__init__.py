@@ -7,7 +7,8 @@ thin ctypes binding over it plus the seeded synthetic-input generator.
 from . import _build
 from .binding import (ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG, ATTN_ERR_NO_DEVICE, ATTN_ERR_TIMEOUT,
                       ATTN_ERR_UNSUPPORTED, ATTN_OK, EXPORTS, AttnError, attn_check_device,
-                      attn_decode_workspace_bytes, attn_fwd, attn_fwd_raw, attn_status_string,
+                      attn_decode_workspace_bytes, attn_fwd, attn_fwd_raw, attn_last_cuda_error,
+                      attn_status_string,
                       attn_version, load_library)
 
 
@@ -19,6 +20,6 @@ def build(force: bool = False) -> str:
 
 
 __all__ = ["build", "attn_fwd", "attn_fwd_raw", "attn_check_device", "attn_status_string",
-           "attn_version", "attn_decode_workspace_bytes", "AttnError", "load_library", "EXPORTS",
+           "attn_version", "attn_decode_workspace_bytes", "attn_last_cuda_error", "AttnError", "load_library", "EXPORTS",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
            "ATTN_ERR_TIMEOUT", "ATTN_ERR_NO_DEVICE"]

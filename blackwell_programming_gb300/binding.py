@@ -73,6 +73,10 @@ def attn_status_string(status: int) -> str:
     return load_library().attn_status_string(status).decode()
 
 
+def attn_last_cuda_error() -> str:
+    return load_library().attn_last_cuda_error().decode()
+
+
 def attn_version() -> int:
     return load_library().attn_version()
 

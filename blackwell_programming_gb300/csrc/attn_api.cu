@@ -22,7 +22,9 @@
 
 namespace gbattn {
 
-__device__ unsigned g_device_error = 0u;
+// Error bits in [0]; the first timed-out wait's block, warp, barrier and
+// parity in [1..4].
+__device__ unsigned g_device_error[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 
 namespace {
 
@@ -114,15 +116,19 @@ bool check_env() {
 }
 
 int read_device_error(cudaStream_t stream, unsigned* err, int reset) {
-  unsigned h = 0;
-  cudaError_t e = cudaMemcpyAsync(&h, err, sizeof(h), cudaMemcpyDeviceToHost, stream);
+  unsigned h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+  cudaError_t e = cudaMemcpyAsync(h, err, sizeof(h), cudaMemcpyDeviceToHost, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(error word)");
   if (reset) {
-    if ((e = cudaMemsetAsync(err, 0, sizeof(unsigned), stream)) != cudaSuccess)
+    if ((e = cudaMemsetAsync(err, 0, sizeof(h), stream)) != cudaSuccess)
       return cuda_fail(e, "cudaMemsetAsync(error word)");
   }
   if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-  return h ? ATTN_ERR_TIMEOUT : ATTN_OK;
+  if (h[0] == 0u) return ATTN_OK;
+  std::snprintf(t_cuda_error, sizeof(t_cuda_error),
+                "a kernel wait gave up: block %u warp %u barrier at shared offset 0x%x parity %u", h[1], h[2],
+                h[3], h[4]);
+  return ATTN_ERR_TIMEOUT;
 }
 
 }  // namespace

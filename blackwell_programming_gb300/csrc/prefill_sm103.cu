@@ -288,11 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (++vs == C::VS) { vs = 0; vph ^= 1u; }
           }
         }
+        // A tile with no K/V tile still takes one o_empty / o_full turn, so
+        // its epilogue can never run a barrier phase ahead of this warp.
         for (int t = 0; t < 2 && ok; ++t) {
           if (!o_waited[t]) {
             if (!(ok = mbar_wait(bar(C::B_OEMPTY + t), oeph[t] ^ 1u, wctx))) break;
             oeph[t] ^= 1u;
           }
+          if (U.n[t] == 0) mma_commit(bar(C::B_OFULL + t));
         }
         if (!ok) break;
       }
@@ -387,11 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // epilogue: O / l and LSE, then hand O_t back to the MMA warp
-      if (n > 0) {
-        if (!(ok = warp_wait(bar(C::B_OFULL + t), ofph, wctx))) break;
-        ofph ^= 1u;
-        tc_fence_after();
-      }
+      if (!(ok = warp_wait(bar(C::B_OFULL + t), ofph, wctx))) break;
+      ofph ^= 1u;
+      tc_fence_after();
       const bool live = row < p.Nq;
       float* orow = p.o + (static_cast<size_t>(U.b * p.Hq + U.h) * p.Nq + (live ? row : 0)) * D;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;

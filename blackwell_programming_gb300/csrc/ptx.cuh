@@ -66,10 +66,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Shared state that lets every role of a CTA stop early once one of them has
 // given up on a wait: `abort_flag` lives in shared memory, `err` in global.
+// err[0] holds the error bits; err[1..4] record the first wait that gave up
+// (block, warp, barrier byte offset in shared memory, parity).
 struct WaitCtx {
   volatile uint32_t* abort_flag;
   unsigned* err;
 };
+
+__device__ __forceinline__ void record_timeout(const WaitCtx& w, uint32_t bar, uint32_t parity) {
+  *w.abort_flag = 1u;
+  if (atomicOr(w.err, kErrTimeout) == 0u) {
+    w.err[1] = blockIdx.x;
+    w.err[2] = threadIdx.x >> 5;
+    w.err[3] = bar;
+    w.err[4] = parity;
+  }
+}
 
 // Wait until the phase with parity `parity` of barrier `bar` has completed.
 // Returns false (and flags the CTA and the device error word) on timeout, or
@@ -82,8 +94,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     if ((it & 63u) == 0u) {
       if (*w.abort_flag) return false;
       if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-        *w.abort_flag = 1u;
-        atomicOr(w.err, kErrTimeout);
+        record_timeout(w, bar, parity);
         return false;
       }
     }

@@ -28,9 +28,11 @@ def run_gpu(inp, stream=None):
     import blackwell_programming_gb300 as gb
     wl = inp.wl
     q, k, v = to_torch(inp)
+    gb.attn_check_device(reset=True)
     o, lse = gb.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, stream=stream)
     torch.cuda.synchronize()
-    assert gb.attn_check_device() == 0
+    st = gb.attn_check_device(reset=True)
+    assert st == 0, "device status %d (%s): %s" % (st, gb.attn_status_string(st), gb.attn_last_cuda_error())
     return o, lse
 
 
