@@ -19,10 +19,11 @@ ATTN_ERR_UNSUPPORTED = 2
 ATTN_ERR_CUDA = 3
 ATTN_ERR_TIMEOUT = 4
 ATTN_ERR_NO_DEVICE = 5
+ATTN_ERR_SCRATCH_LIMIT = 6
 
 # Symbols the shared library exports (the declarations of include/gbattn.h).
 EXPORTS = ("attn_fwd", "attn_check_device", "attn_status_string", "attn_last_cuda_error",
-           "attn_version", "attn_decode_workspace_bytes")
+           "attn_version", "attn_decode_workspace_bytes", "attn_decode_fwd_noalloc")
 
 _lib = None
 
@@ -56,6 +57,8 @@ def load_library(path: str | None = None):
     L.attn_version.restype = i
     L.attn_decode_workspace_bytes.argtypes = [i, i, i]
     L.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+    L.attn_decode_fwd_noalloc.argtypes = [vp, vp, vp, vp, i, i, i, i, f, vp]
+    L.attn_decode_fwd_noalloc.restype = i
     if path == _build.LIB:
         _lib = L
     return L
@@ -83,6 +86,23 @@ def attn_version() -> int:
 
 def attn_decode_workspace_bytes(B: int, Hkv: int, Nkv: int) -> int:
     return load_library().attn_decode_workspace_bytes(B, Hkv, Nkv)
+
+
+# Size of the static scratch array behind attn_decode_fwd_noalloc (see gbattn.h).
+NOALLOC_SCRATCH_BYTES = 48 << 20
+
+
+def attn_decode_fwd_noalloc(q_ptr: int, kv_ptr: int, o_ptr: int, lse_ptr: int, B: int, Hq: int, Hkv: int,
+                            Nkv: int, scale: float, stream_ptr: int = 0) -> int:
+    """The allocation-free decode call with raw integer pointers; returns the status code.
+
+    For callers that cannot let the library allocate device memory: the
+    split partials go to the library's fixed static scratch array.
+    """
+    L = load_library()
+    return L.attn_decode_fwd_noalloc(ctypes.c_void_p(q_ptr), ctypes.c_void_p(kv_ptr), ctypes.c_void_p(o_ptr),
+                                     ctypes.c_void_p(lse_ptr), B, Hq, Hkv, Nkv, ctypes.c_float(scale),
+                                     ctypes.c_void_p(stream_ptr))
 
 
 def _stream_handle(stream, device):

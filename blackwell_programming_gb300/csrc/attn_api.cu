@@ -148,6 +148,7 @@ const char* attn_status_string(int status) {
     case ATTN_ERR_CUDA: return "CUDA error";
     case ATTN_ERR_TIMEOUT: return "kernel wait timed out";
     case ATTN_ERR_NO_DEVICE: return "no sm_103 device";
+    case ATTN_ERR_SCRATCH_LIMIT: return "problem needs more than the fixed static scratch";
     default: return "unknown status";
   }
 }
@@ -269,3 +270,93 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// attn_decode_fwd_noalloc: the split-KV decode without any allocation.
+//
+// Its partial results live in one fixed array in device memory, declared
+// here at file scope.  Every GPU that loads this library holds the array
+// until the process exits; all calls on a device share it.
+namespace gbattn {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;   // 48 MiB
+__device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// once per device (with that device current) and cached.
+int noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    float* ptr = nullptr;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace gbattn
+
+extern "C" int attn_decode_fwd_noalloc(const void* q, const void* kv, float* o, float* lse, int B, int Hq, int Hkv,
+                                       int Nkv, float scale, attn_stream_t stream_) {
+  t_cuda_error[0] = '\0';
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (q == nullptr || kv == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq / Hkv > 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hkv * Nkv >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
+
+  DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  float* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != ATTN_OK) return st;
+
+  const int d_qk = 576;
+  const int group = Hq / Hkv;
+  const int planes = B * Hkv;
+  DecodeParams p{};
+  p.planes = planes;
+  p.group = group;
+  p.Nkv = Nkv;
+  p.tiles = decode_tiles(Nkv);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = dev->err;
+  const long long total = 2LL * planes * p.tiles;
+  const int grid = static_cast<int>(std::min<long long>(total, dev->num_sms));
+  p.max_seg = decode_max_segments(planes, p.tiles, grid);
+  const size_t n_slots = static_cast<size_t>(grid) * p.max_seg * 128;
+  if (n_slots * (256 + 1) * sizeof(float) > kNoAllocScratchBytes) {
+    std::snprintf(t_cuda_error, sizeof(t_cuda_error),
+                  "needs %zu bytes of scratch, the static array holds %zu", n_slots * (256 + 1) * sizeof(float),
+                  kNoAllocScratchBytes);
+    return ATTN_ERR_SCRATCH_LIMIT;
+  }
+  CUtensorMap tq, tk;
+  const uint64_t rs = static_cast<uint64_t>(d_qk) * 2;
+  if ((st = make_map(&tq, q, d_qk, group, planes, rs, rs * group, 128)) != ATTN_OK) return st;
+  if ((st = make_map(&tk, kv, d_qk, Nkv, planes, rs, rs * Nkv, 32)) != ATTN_OK) return st;
+  // Every slot the combine kernel reads is written first by the decode
+  // kernel in the same call, so nothing needs clearing between calls.
+  p.o_part = scratch;
+  p.lse_part = scratch + n_slots * 256;
+  cudaError_t e;
+  if ((e = launch_decode(tq, tk, p, grid, stream)) != cudaSuccess) return cuda_fail(e, "decode launch");
+  if ((e = launch_combine(p, grid, o, lse, stream)) != cudaSuccess) return cuda_fail(e, "combine launch");
+  if (check_env()) return read_device_error(stream, dev->err, 0);
+  return ATTN_OK;
+}

@@ -45,7 +45,9 @@ typedef enum {
     ATTN_ERR_UNSUPPORTED = 2,  /* head dims not built, or causal decode shape   */
     ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed             */
     ATTN_ERR_TIMEOUT = 4,      /* a kernel gave up on a bounded wait            */
-    ATTN_ERR_NO_DEVICE = 5     /* no sm_103 device is current                   */
+    ATTN_ERR_NO_DEVICE = 5,    /* no sm_103 device is current                   */
+    ATTN_ERR_SCRATCH_LIMIT = 6 /* attn_decode_fwd_noalloc: problem needs more
+                                  scratch than its fixed static array holds     */
 } attn_status;
 
 /*
@@ -106,6 +108,41 @@ int attn_version(void);
  * arguments are not positive or no sm_103 device is current.
  */
 size_t attn_decode_workspace_bytes(int B, int Hkv, int Nkv);
+
+/*
+ * attn_decode_fwd_noalloc - the (576, 512) split-KV decode of attn_fwd,
+ * without any memory allocation.  The paper has no counterpart; it is a
+ * library service.
+ *
+ * Who needs it: callers that cannot let a library allocate device memory at
+ * call time - a host framework whose caching allocator already holds the
+ * GPU's free memory, a serving loop with a fixed memory budget that must not
+ * fail in the middle of a request, or a plug-in whose host forbids
+ * allocation.  attn_fwd takes its decode workspace from cudaMallocAsync;
+ * this entry point calls no cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Its split partials go to one static device array of 48 MiB declared in
+ * the library.  Every GPU that loads the library holds that array until the
+ * process exits.  Problems whose partials would not fit return
+ * ATTN_ERR_SCRATCH_LIMIT (the 64 x 128-head x 8192-key shape needs about
+ * 40 MB on a 152-SM GB300).
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture.  All calls on a device share the one array and it keeps
+ * the last call's contents; no call relies on it starting at zero.  Calls
+ * whose work overlaps on the GPU (e.g. on two streams at once) race on the
+ * array: serialise them.
+ *
+ *  q   bf16 [B, Hq, 1, 576];  kv bf16 [B, Hkv, Nkv, 576] holding K, with V
+ *      the first 512 features of each row;  o fp32 [B, Hq, 1, 512];
+ *  lse fp32 [B, Hq, 1] or NULL.  Hq / Hkv <= 128.  Same numbers, layouts,
+ *  errors and asynchrony as attn_fwd(q, kv, kv, o, lse, B, Hq, Hkv, 1, Nkv,
+ *  576, 512, 0, scale, stream).
+ */
+int attn_decode_fwd_noalloc(const void* q, const void* kv, float* o, float* lse,
+                            int B, int Hq, int Hkv, int Nkv, float scale,
+                            attn_stream_t stream);
 
 #ifdef __cplusplus
 }
