@@ -332,9 +332,12 @@ def run_ours(args, wl):
     flops = wl.flops
     value = aggregate(flops * args.steps, t_max, world) / 1e12
 
-    e2e_secs, h2d, d2h = measure_e2e(wl, args.steps, args.warmup, stream, (hq, hk, hv))
-    e2e_max = reduce_max(e2e_secs, world)
-    e2e_value = aggregate(flops * args.steps, e2e_max, world) / 1e12
+    e2e = None
+    if not args.no_e2e:
+        e2e_secs, h2d, d2h = measure_e2e(wl, args.steps, args.warmup, stream, (hq, hk, hv))
+        e2e_max = reduce_max(e2e_secs, world)
+        e2e = {"value": aggregate(flops * args.steps, e2e_max, world) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     peaks, peak_src = load_peaks()
     kind = "decode" if wl.d_qk == 576 else "prefill"
@@ -360,8 +363,7 @@ def run_ours(args, wl):
                 "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": workload_config(wl), "roofline": roof, "cpu_baseline": cpu,
-                "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                        "d2h_bytes_per_step": d2h},
+                "e2e": e2e,
                 "gpu_launches": launches, "clocks": clk,
                 "step_ms": {"min": min(times) * 1e3, "median": statistics.median(times) * 1e3,
                             "max": max(times) * 1e3}}
@@ -381,9 +383,13 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size (profiling cases)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)      # at least three untimed warm-up steps
     wl = syn.WORKLOADS[args.workload]
+    if args.batch is not None:
+        wl = wl.with_sizes(B=args.batch, name="%s_B%d" % (wl.name, args.batch))
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -44,6 +44,12 @@ constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only past 2^8
 constexpr uint32_t kFull = 0xFFFFFFFFu;
+// Register split: the MMA / TMA warpgroup gives registers to the two softmax
+// warpgroups.  128 * 96 + 256 * 200 = 63488 must not exceed the launch
+// allocation (384 threads x registers per thread), which the host checks.
+constexpr uint32_t kRegsLow = 96;
+constexpr uint32_t kRegsHigh = 200;
+constexpr int kRegsNeededAtLaunch = (128 * kRegsLow + 256 * kRegsHigh + kThreads - 1) / kThreads;
 
 template <int D>
 struct Cfg {
@@ -158,8 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
-
-  if (warp == kTmaWarp) {
+  if (warp >= 8) {
+   regs_dec<kRegsLow>();
+   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -169,10 +176,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_q = l2_policy_evict_first();
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0, qph[2] = {0, 0};
-      int k_last[C::KS], v_last[C::VS];   // parity of the last fill of each stage, -1 = none
-      int q_last[2] = {-1, -1};
-      for (int s = 0; s < C::KS; ++s) k_last[s] = -1;
-      for (int s = 0; s < C::VS; ++s) v_last[s] = -1;
+      // Buffers filled so far (bit b) and the parity of their last fill, for
+      // the drain at exit.  Bits: Q tile t -> t, K stage s -> 2 + s,
+      // V stage s -> 2 + KS + s.
+      uint32_t filled = 0u, fill_par = 0u;
+      auto note_fill = [&](int b, uint32_t par) {
+        filled |= 1u << b;
+        fill_par = (fill_par & ~(1u << b)) | (par << b);
+      };
       const int group = p.Hq / p.Hkv;
       for (int it = 0;; ++it) {
         const int u = unit_at(it);
@@ -184,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(bar(C::B_QEMPTY + t), qph[t] ^ 1u, wctx))) break;
           qph[t] ^= 1u;
           mbar_arrive_expect_tx(bar(C::B_QFULL + t), C::Q_BYTES);
-          q_last[t] = static_cast<int>(qph[t] ^ 1u);
+          note_fill(t, qph[t] ^ 1u);
           for (int kc = 0; kc < C::KCH; ++kc)
             tma_load_3d(sQ + t * C::Q_BYTES + kc * C::CHUNK_Q, &tmQ, bar(C::B_QFULL + t), kc * 64,
                         (U.qb * 2 + t) * BM, U.b * p.Hq + U.h, pol_q);
@@ -195,14 +206,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < nmax && ok; ++j) {
           if (!(ok = mbar_wait(bar(C::B_KEMPTY + ks), kph ^ 1u, wctx))) break;
           mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::KV_BYTES);
-          k_last[ks] = static_cast<int>(kph);
+          note_fill(2 + ks, kph);
           for (int kc = 0; kc < C::KCH; ++kc)
             tma_load_3d(sK + ks * C::KV_BYTES + kc * C::CHUNK_KV, &tmK, bar(C::B_KFULL + ks), kc * 64, j * BN,
                         z, pol_kv);
           if (++ks == C::KS) { ks = 0; kph ^= 1u; }
           if (!(ok = mbar_wait(bar(C::B_VEMPTY + vs), vph ^ 1u, wctx))) break;
           mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::KV_BYTES);
-          v_last[vs] = static_cast<int>(vph);
+          note_fill(2 + C::KS + vs, vph);
           for (int kc = 0; kc < C::KCH; ++kc)
             tma_load_3d(sV + vs * C::KV_BYTES + kc * C::CHUNK_KV, &tmV, bar(C::B_VFULL + vs), kc * 64, j * BN,
                         z, pol_kv);
@@ -211,15 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
       // Every issued copy must have landed before the CTA may exit.
-      for (int t = 0; t < 2; ++t)
-        if (q_last[t] >= 0) mbar_wait_drain(bar(C::B_QFULL + t), static_cast<uint32_t>(q_last[t]));
-      for (int s = 0; s < C::KS; ++s)
-        if (k_last[s] >= 0) mbar_wait_drain(bar(C::B_KFULL + s), static_cast<uint32_t>(k_last[s]));
-      for (int s = 0; s < C::VS; ++s)
-        if (v_last[s] >= 0) mbar_wait_drain(bar(C::B_VFULL + s), static_cast<uint32_t>(v_last[s]));
+      for (int b = 0; b < 2 + C::KS + C::VS; ++b) {
+        if (!((filled >> b) & 1u)) continue;
+        const int full = b < 2 ? C::B_QFULL + b : (b < 2 + C::KS ? C::B_KFULL + (b - 2) : C::B_VFULL + (b - 2 - C::KS));
+        mbar_wait_drain(bar(full), (fill_par >> b) & 1u);
+      }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------- MMA issuer
     if (lane == 0) {
       int ks = 0, vs = 0;
@@ -304,7 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(bar(C::B_DRAIN), 0);
     }
     __syncwarp();
-  } else if (warp < 8) {
+   }
+  } else {
+    regs_inc<kRegsHigh>();
     // ------------------------------------------------ softmax + epilogue
     const int t = static_cast<int>(warp >> 2);
     const uint32_t quad = warp & 3u;
@@ -331,20 +343,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key0 = j * BN;
         const bool need_mask = (key0 + BN > p.Nkv) || (p.causal && key0 + BN - 1 > q0 + delta);
         const int key_lim = p.causal ? min(row + delta, p.Nkv - 1) : p.Nkv - 1;   // last visible key
-        // pass 1: row maximum of the raw logits
-        float mx = -INFINITY;
+        // The whole 128-column S row in registers: one TMEM load per tile.
+        float v[BN];
+        tmem_ld128(tS, v);
+        if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(tS + c * 32, v);
-          if (need_mask) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (key0 + c * 32 + i > key_lim) v[i] = -INFINITY;
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
+          for (int i = 0; i < BN; ++i)
+            if (key0 + i > key_lim) v[i] = -INFINITY;
         }
+        // Row maximum: eight independent three-input max chains, then merge.
+        float mx8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(v[2 * a], v[2 * a + 1]);
+#pragma unroll
+        for (int i = 8; i < BN / 2; ++i) mx8[i & 7] = fmax3(mx8[i & 7], v[2 * i], v[2 * i + 1]);
+        const float mx = fmaxf(fmax3(fmax3(mx8[0], mx8[1], mx8[2]), mx8[3], mx8[4]),
+                               fmax3(mx8[5], mx8[6], mx8[7]));
         const float m_new = (mx == -INFINITY) ? -INFINITY : mx * sl2;
         float alpha = 1.f;
         const bool grow = m_new > m_used + kRescaleThreshold;
@@ -364,25 +378,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float base = (m_used == -INFINITY) ? 0.f : m_used;
-        // pass 2: P = 2^(s * scale * log2 e - m), row sum, P as bf16 over S
+        // P = 2^(s * scale * log2 e - m): the argument with paired FMAs, the
+        // exponential on the SFU, the row sum in four paired accumulators,
+        // P as bf16 pairs written over S.
+        const uint64_t c2 = f2_pack(sl2, sl2);
+        const uint64_t nb2 = f2_pack(-base, -base);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[BN / 2];
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          float v[32];
-          tmem_ld32(tS + c * 32, v);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float p0 = ex2(fmaf(v[2 * i], sl2, -base));
-            float p1 = ex2(fmaf(v[2 * i + 1], sl2, -base));
-            if (need_mask) {
-              if (key0 + c * 32 + 2 * i > key_lim) p0 = 0.f;
-              if (key0 + c * 32 + 2 * i + 1 > key_lim) p1 = 0.f;
-            }
-            l += p0 + p1;
-            pk[i] = pack_bf16x2(p0, p1);
+        for (int i = 0; i < BN / 2; ++i) {
+          const uint64_t x = f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), c2, nb2);
+          float p0 = ex2(f2_lo(x));
+          float p1 = ex2(f2_hi(x));
+          if (need_mask) {
+            if (key0 + 2 * i > key_lim) p0 = 0.f;
+            if (key0 + 2 * i + 1 > key_lim) p1 = 0.f;
           }
-          tmem_st16(tS + c * 16, pk);
+          acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);
         }
+        tmem_st64(tS, pk);
+        const uint64_t a01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+        l += f2_lo(a01) + f2_hi(a01);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -439,6 +456,11 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   if (e != cudaSuccess) return e;
   const int grid = min(p.num_units, num_sms);
   if (grid <= 0) return cudaSuccess;
+  // The register split needs the kernel to be launched with enough registers;
+  // otherwise setmaxnreg.inc could never be served, so refuse to launch.
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, prefill_kernel<D>)) != cudaSuccess) return e;
+  if (((fa.numRegs + 7) / 8) * 8 < kRegsNeededAtLaunch) return cudaErrorInvalidConfiguration;
   prefill_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
