@@ -18,11 +18,11 @@
 //    (expect-tx on full, tcgen05.commit on empty) - the producer/consumer
 //    template of "Distilling...", section 12, with the mbarrier handoff of
 //    section 13.
-//  * Warp 8 issues every tcgen05.mma from one thread.  S_t = Q_t K_j^T lands
-//    in tensor memory (TMEM); the softmax writes P_t (bf16) over S_t and the
-//    MMA computes O_t += P_t V_j with P read straight from TMEM.  The two
-//    query tiles ping-pong: the tensor core works on one tile while the
-//    softmax warpgroup of the other one runs.
+//  * Warps 8 and 10 issue the tcgen05.mma of query tile 0 and 1, one thread
+//    each.  S_t = Q_t K_j^T lands in tensor memory (TMEM); the softmax writes
+//    P_t (bf16) over S_t and the MMA computes O_t += P_t V_j with P read
+//    straight from TMEM.  The two query tiles ping-pong: the tensor core
+//    works on one tile while the softmax warpgroup of the other one runs.
 //  * Warpgroups 0 and 1 own query tile 0 and 1.  TMEM lane i is row i, so a
 //    thread owns a whole row: max, exp2 and sum stay in-thread.  They also
 //    rescale O (only when the running max grew by more than 2^8, which keeps
@@ -40,8 +40,9 @@ namespace {
 constexpr int BM = 128;               // query rows per tile (TMEM lanes)
 constexpr int BN = 128;               // keys per K/V tile
 constexpr int kThreads = 384;         // 3 warpgroups
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarp0 = 8;    // MMA issuer for query tile 0 (also owns the TMEM allocation)
 constexpr int kTmaWarp = 9;
+constexpr int kMmaWarp1 = 10;   // MMA issuer for query tile 1
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only past 2^8
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 // Register split: the MMA / TMA warpgroup gives registers to the two softmax
@@ -68,7 +69,7 @@ struct Cfg {
   static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 4 + KS, B_VFULL = 4 + 2 * KS,
                        B_VEMPTY = 4 + 2 * KS + VS, B_SFULL = 4 + 2 * KS + 2 * VS, B_PFULL = B_SFULL + 2,
                        B_OFULL = B_PFULL + 2, B_OEMPTY = B_OFULL + 2, B_DRAIN = B_OEMPTY + 2,
-                       NUM_BARS = B_DRAIN + 1;
+                       B_TURN = B_DRAIN + 1, NUM_BARS = B_TURN + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alignment
   // TMEM column of S_t and O_t
@@ -147,16 +148,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < C::KS; ++s) {
       mbar_init(bar(C::B_KFULL + s), 1);
-      mbar_init(bar(C::B_KEMPTY + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), 2);   // released by both MMA warps
     }
     for (int s = 0; s < C::VS; ++s) {
       mbar_init(bar(C::B_VFULL + s), 1);
-      mbar_init(bar(C::B_VEMPTY + s), 1);
+      mbar_init(bar(C::B_VEMPTY + s), 2);
     }
-    mbar_init(bar(C::B_DRAIN), 1);
+    mbar_init(bar(C::B_DRAIN), 2);
+    mbar_init(bar(C::B_TURN + 0), 1);
+    mbar_init(bar(C::B_TURN + 1), 1);
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -229,66 +232,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-   } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------- MMA issuer
+   } else if (warp == kMmaWarp0 || warp == kMmaWarp1) {
+    // --------------------------------------------------------- MMA issuers
+    // One issuing warp per query tile.  tcgen05.mma issue blocks while the
+    // tensor core's queue is full, so a single issuer leaves the tensor core
+    // idle whenever it waits on a barrier; with two, one tile's issuer waits
+    // for its P while the other issues.  The two pass an issue turn (a pair
+    // of mbarriers) once per K/V step, so the tensor core runs tile 0's
+    // group [PV_0, S_0] and then tile 1's [PV_1, S_1]: the tiles stay half a
+    // period apart and each softmax overlaps the other tile's MMAs instead
+    // of running at the same time.  Both walk the same K/V stages and both
+    // release each stage (empty barriers count 2).
+    const int t = (warp == kMmaWarp0) ? 0 : 1;
     if (lane == 0) {
       int ks = 0, vs = 0;
-      uint32_t kph = 0, vph = 0, qph[2] = {0, 0}, pph[2] = {0, 0}, oeph[2] = {0, 0};
+      uint32_t kph = 0, vph = 0, qph = 0, pph = 0, oeph = 0;
+      // Tile 0 holds the turn first: its first wait is on the phase before
+      // the barrier's first one, which counts as complete.
+      uint32_t tph = (t == 0) ? 1u : 0u;
+      const uint32_t dS = tm + C::col_s(t), dO = tm + C::col_o(t);
+      const uint32_t qbase = sQ + t * C::Q_BYTES;
       for (int it = 0;; ++it) {
         const int u = unit_at(it);
         if (u >= p.num_units) break;
         const Unit U = decode_unit(u, p);
+        const int n = U.n[t];
         const int nmax = max(U.n[0], U.n[1]);
-        bool o_waited[2] = {false, false};
+        bool o_waited = false;
         bool ok = true;
         for (int j = 0; j <= nmax && ok; ++j) {
-          if (j < nmax) {
-            if (!(ok = mbar_wait(bar(C::B_KFULL + ks), kph, wctx))) break;
+          const bool do_pv = j >= 1 && j - 1 < n;
+          const bool do_s = j < n;
+          // every wait of this step first, then the turn
+          if (j >= 1 && !(ok = mbar_wait(bar(C::B_VFULL + vs), vph, wctx))) break;
+          if (j < nmax && !(ok = mbar_wait(bar(C::B_KFULL + ks), kph, wctx))) break;
+          if (do_pv) {
+            if (!o_waited) {
+              if (!(ok = mbar_wait(bar(C::B_OEMPTY + t), oeph ^ 1u, wctx))) break;
+              oeph ^= 1u;
+              o_waited = true;
+            }
+            if (!(ok = mbar_wait(bar(C::B_PFULL + t), pph, wctx))) break;
+            pph ^= 1u;
           }
-          if (j >= 1) {
-            if (!(ok = mbar_wait(bar(C::B_VFULL + vs), vph, wctx))) break;
+          if (do_s && j == 0) {
+            if (!(ok = mbar_wait(bar(C::B_QFULL + t), qph, wctx))) break;
+            qph ^= 1u;
           }
+          if (!(ok = mbar_wait(bar(C::B_TURN + t), tph, wctx))) break;
+          tph ^= 1u;
           tc_fence_after();
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j >= 1 && j - 1 < U.n[t]) {
-              if (!o_waited[t]) {
-                if (!(ok = mbar_wait(bar(C::B_OEMPTY + t), oeph[t] ^ 1u, wctx))) break;
-                oeph[t] ^= 1u;
-                o_waited[t] = true;
-              }
-              if (!(ok = mbar_wait(bar(C::B_PFULL + t), pph[t], wctx))) break;
-              pph[t] ^= 1u;
-              tc_fence_after();
-              const uint32_t vbase = sV + vs * C::KV_BYTES;
+          if (do_pv) {
+            // O_t += P_t(j-1) V_{j-1}; P read from TMEM over S_t
+            const uint32_t vbase = sV + vs * C::KV_BYTES;
 #pragma unroll
-              for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint64_t bdesc = smem_desc_sw128(vbase + kk * 16 * 128, C::CHUNK_KV, 1024);
-                mma_ts(tm + C::col_o(t), tm + C::col_s(t) + kk * 8, bdesc, C::IDESC_PV,
-                       (j - 1 > 0 || kk > 0) ? 1u : 0u);
-              }
-            }
-            if (j < U.n[t]) {
-              if (j == 0) {
-                if (!(ok = mbar_wait(bar(C::B_QFULL + t), qph[t], wctx))) break;
-                qph[t] ^= 1u;
-                tc_fence_after();
-              }
-              const uint32_t qbase = sQ + t * C::Q_BYTES;
-              const uint32_t kbase = sK + ks * C::KV_BYTES;
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ts(dO, dS + kk * 8, smem_desc_sw128(vbase + kk * 16 * 128, C::CHUNK_KV, 1024), C::IDESC_PV,
+                     (j - 1 > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (do_s) {
+            // S_t = Q_t K_j^T
+            const uint32_t kbase = sK + ks * C::KV_BYTES;
 #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off_q = (kk >> 2) * C::CHUNK_Q + (kk & 3) * 32;
-                const uint32_t off_k = (kk >> 2) * C::CHUNK_KV + (kk & 3) * 32;
-                mma_ss(tm + C::col_s(t), smem_desc_sw128(qbase + off_q, 16, 1024),
-                       smem_desc_sw128(kbase + off_k, 16, 1024), C::IDESC_S, kk > 0 ? 1u : 0u);
-              }
-              mma_commit(bar(C::B_SFULL + t));
-              if (j == U.n[t] - 1) mma_commit(bar(C::B_QEMPTY + t));
-            } else if (j == U.n[t] && U.n[t] > 0) {
-              mma_commit(bar(C::B_OFULL + t));
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off_q = (kk >> 2) * C::CHUNK_Q + (kk & 3) * 32;
+              const uint32_t off_k = (kk >> 2) * C::CHUNK_KV + (kk & 3) * 32;
+              mma_ss(dS, smem_desc_sw128(qbase + off_q, 16, 1024), smem_desc_sw128(kbase + off_k, 16, 1024),
+                     C::IDESC_S, kk > 0 ? 1u : 0u);
             }
           }
-          if (!ok) break;
+          mbar_arrive(bar(C::B_TURN + (t ^ 1)));
+          if (do_s) {
+            mma_commit(bar(C::B_SFULL + t));
+            if (j == n - 1) mma_commit(bar(C::B_QEMPTY + t));
+          }
+          if (j == n && n > 0) mma_commit(bar(C::B_OFULL + t));
           if (j < nmax) {
             mma_commit(bar(C::B_KEMPTY + ks));
             if (++ks == C::KS) { ks = 0; kph ^= 1u; }
@@ -298,18 +316,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (++vs == C::VS) { vs = 0; vph ^= 1u; }
           }
         }
+        if (!ok) break;
         // A tile with no K/V tile still takes one o_empty / o_full turn, so
         // its epilogue can never run a barrier phase ahead of this warp.
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (!o_waited[t]) {
-            if (!(ok = mbar_wait(bar(C::B_OEMPTY + t), oeph[t] ^ 1u, wctx))) break;
-            oeph[t] ^= 1u;
-          }
-          if (U.n[t] == 0) mma_commit(bar(C::B_OFULL + t));
+        if (!o_waited) {
+          if (!(ok = mbar_wait(bar(C::B_OEMPTY + t), oeph ^ 1u, wctx))) break;
+          oeph ^= 1u;
         }
-        if (!ok) break;
+        if (n == 0) mma_commit(bar(C::B_OFULL + t));
       }
-      // Let every issued MMA finish before TMEM is released.
+      // Let every MMA this warp issued finish before TMEM is released.
       mma_commit(bar(C::B_DRAIN));
       mbar_wait_drain(bar(C::B_DRAIN), 0);
     }
@@ -441,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     tc_fence_after();
     tmem_dealloc(tm, 512);
   }
