@@ -18,10 +18,10 @@
 //    (expect-tx on full, tcgen05.commit on empty) - the producer/consumer
 //    template of "Distilling...", section 12, with the mbarrier handoff of
 //    section 13.
-//  * Warps 8 and 10 issue the tcgen05.mma of query tile 0 and 1, one thread
-//    each.  S_t = Q_t K_j^T lands in tensor memory (TMEM); the softmax writes
-//    P_t (bf16) over S_t and the MMA computes O_t += P_t V_j with P read
-//    straight from TMEM.  The two query tiles ping-pong: the tensor core
+//  * Warps 8 and 10 issue the tcgen05.mma of query tile 0 and 1 (warp-uniform
+//    code, one elected lane per instruction).  S_t = Q_t K_j^T lands in
+//    tensor memory (TMEM); the softmax writes P_t (bf16) over S_t and the
+//    MMA computes O_t += P_t V_j with P read straight from TMEM.  The two query tiles ping-pong: the tensor core
 //    works on one tile while the softmax warpgroup of the other one runs.
 //  * Warpgroups 0 and 1 own query tile 0 and 1.  TMEM lane i is row i, so a
 //    thread owns a whole row: max, exp2 and sum stay in-thread.  They also
@@ -244,14 +244,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of running at the same time.  Both walk the same K/V stages and both
     // release each stage (empty barriers count 2).
     const int t = (warp == kMmaWarp0) ? 0 : 1;
-    if (lane == 0) {
+    // The whole warp runs this loop (warp-uniform control flow); one elected
+    // lane issues each tcgen05 instruction.
+    {
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0, qph = 0, pph = 0, oeph = 0;
       // Tile 0 holds the turn first: its first wait is on the phase before
       // the barrier's first one, which counts as complete.
       uint32_t tph = (t == 0) ? 1u : 0u;
       const uint32_t dS = tm + C::col_s(t), dO = tm + C::col_o(t);
-      const uint32_t qbase = sQ + t * C::Q_BYTES;
+      // Base descriptors; a K step adds its byte offset / 16 to the start
+      // address field (offsets stay inside the 256 KB window).
+      const uint64_t q_desc = smem_desc_sw128(sQ + t * C::Q_BYTES, 16, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(sK, 16, 1024);
+      const uint64_t v_desc0 = smem_desc_sw128(sV, C::CHUNK_KV, 1024);
       for (int it = 0;; ++it) {
         const int u = unit_at(it);
         if (u >= p.num_units) break;
@@ -264,55 +270,53 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool do_pv = j >= 1 && j - 1 < n;
           const bool do_s = j < n;
           // every wait of this step first, then the turn
-          if (j >= 1 && !(ok = mbar_wait(bar(C::B_VFULL + vs), vph, wctx))) break;
-          if (j < nmax && !(ok = mbar_wait(bar(C::B_KFULL + ks), kph, wctx))) break;
+          if (j >= 1 && !(ok = warp_wait(bar(C::B_VFULL + vs), vph, wctx))) break;
+          if (j < nmax && !(ok = warp_wait(bar(C::B_KFULL + ks), kph, wctx))) break;
           if (do_pv) {
             if (!o_waited) {
-              if (!(ok = mbar_wait(bar(C::B_OEMPTY + t), oeph ^ 1u, wctx))) break;
+              if (!(ok = warp_wait(bar(C::B_OEMPTY + t), oeph ^ 1u, wctx))) break;
               oeph ^= 1u;
               o_waited = true;
             }
-            if (!(ok = mbar_wait(bar(C::B_PFULL + t), pph, wctx))) break;
+            if (!(ok = warp_wait(bar(C::B_PFULL + t), pph, wctx))) break;
             pph ^= 1u;
           }
           if (do_s && j == 0) {
-            if (!(ok = mbar_wait(bar(C::B_QFULL + t), qph, wctx))) break;
+            if (!(ok = warp_wait(bar(C::B_QFULL + t), qph, wctx))) break;
             qph ^= 1u;
           }
-          if (!(ok = mbar_wait(bar(C::B_TURN + t), tph, wctx))) break;
+          if (!(ok = warp_wait(bar(C::B_TURN + t), tph, wctx))) break;
           tph ^= 1u;
           tc_fence_after();
           if (do_pv) {
             // O_t += P_t(j-1) V_{j-1}; P read from TMEM over S_t
-            const uint32_t vbase = sV + vs * C::KV_BYTES;
+            const uint64_t vd = v_desc0 + ((vs * C::KV_BYTES) >> 4);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ts(dO, dS + kk * 8, smem_desc_sw128(vbase + kk * 16 * 128, C::CHUNK_KV, 1024), C::IDESC_PV,
-                     (j - 1 > 0 || kk > 0) ? 1u : 0u);
+              mma_ts_warp(dO, dS + kk * 8, vd + ((kk * 16 * 128) >> 4), C::IDESC_PV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
           }
           if (do_s) {
             // S_t = Q_t K_j^T
-            const uint32_t kbase = sK + ks * C::KV_BYTES;
+            const uint64_t kd = k_desc0 + ((ks * C::KV_BYTES) >> 4);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off_q = (kk >> 2) * C::CHUNK_Q + (kk & 3) * 32;
-              const uint32_t off_k = (kk >> 2) * C::CHUNK_KV + (kk & 3) * 32;
-              mma_ss(dS, smem_desc_sw128(qbase + off_q, 16, 1024), smem_desc_sw128(kbase + off_k, 16, 1024),
-                     C::IDESC_S, kk > 0 ? 1u : 0u);
+              const uint32_t off_q = ((kk >> 2) * C::CHUNK_Q + (kk & 3) * 32) >> 4;
+              const uint32_t off_k = ((kk >> 2) * C::CHUNK_KV + (kk & 3) * 32) >> 4;
+              mma_ss_warp(dS, q_desc + off_q, kd + off_k, C::IDESC_S, kk > 0 ? 1u : 0u);
             }
           }
-          mbar_arrive(bar(C::B_TURN + (t ^ 1)));
+          mbar_arrive_warp(bar(C::B_TURN + (t ^ 1)));
           if (do_s) {
-            mma_commit(bar(C::B_SFULL + t));
-            if (j == n - 1) mma_commit(bar(C::B_QEMPTY + t));
+            mma_commit_warp(bar(C::B_SFULL + t));
+            if (j == n - 1) mma_commit_warp(bar(C::B_QEMPTY + t));
           }
-          if (j == n && n > 0) mma_commit(bar(C::B_OFULL + t));
+          if (j == n && n > 0) mma_commit_warp(bar(C::B_OFULL + t));
           if (j < nmax) {
-            mma_commit(bar(C::B_KEMPTY + ks));
+            mma_commit_warp(bar(C::B_KEMPTY + ks));
             if (++ks == C::KS) { ks = 0; kph ^= 1u; }
           }
           if (j >= 1) {
-            mma_commit(bar(C::B_VEMPTY + vs));
+            mma_commit_warp(bar(C::B_VEMPTY + vs));
             if (++vs == C::VS) { vs = 0; vph ^= 1u; }
           }
         }
@@ -320,13 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // A tile with no K/V tile still takes one o_empty / o_full turn, so
         // its epilogue can never run a barrier phase ahead of this warp.
         if (!o_waited) {
-          if (!(ok = mbar_wait(bar(C::B_OEMPTY + t), oeph ^ 1u, wctx))) break;
+          if (!(ok = warp_wait(bar(C::B_OEMPTY + t), oeph ^ 1u, wctx))) break;
           oeph ^= 1u;
         }
-        if (n == 0) mma_commit(bar(C::B_OFULL + t));
+        if (n == 0) mma_commit_warp(bar(C::B_OFULL + t));
       }
       // Let every MMA this warp issued finish before TMEM is released.
-      mma_commit(bar(C::B_DRAIN));
+      mma_commit_warp(bar(C::B_DRAIN));
       mbar_wait_drain(bar(C::B_DRAIN), 0);
     }
     __syncwarp();
