@@ -237,8 +237,9 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, 
     CUtensorMap tq, tk;
     const uint64_t rs = static_cast<uint64_t>(d_qk) * 2;
     if ((st = make_map(&tq, q, d_qk, group, planes, rs, rs * group, 128)) != ATTN_OK) return st;
-    if ((st = make_map(&tk, k, d_qk, Nkv, planes, rs, rs * Nkv, 32)) != ATTN_OK) return st;
+    if ((st = make_map(&tk, k, d_qk, Nkv, planes, rs, rs * Nkv, decode_key_tile())) != ATTN_OK) return st;
     DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q);
     p.planes = planes;
     p.group = group;
     p.Nkv = Nkv;
@@ -330,6 +331,7 @@ extern "C" int attn_decode_fwd_noalloc(const void* q, const void* kv, float* o, 
   const int group = Hq / Hkv;
   const int planes = B * Hkv;
   DecodeParams p{};
+  p.q = static_cast<const uint16_t*>(q);
   p.planes = planes;
   p.group = group;
   p.Nkv = Nkv;
@@ -349,7 +351,7 @@ extern "C" int attn_decode_fwd_noalloc(const void* q, const void* kv, float* o, 
   CUtensorMap tq, tk;
   const uint64_t rs = static_cast<uint64_t>(d_qk) * 2;
   if ((st = make_map(&tq, q, d_qk, group, planes, rs, rs * group, 128)) != ATTN_OK) return st;
-  if ((st = make_map(&tk, kv, d_qk, Nkv, planes, rs, rs * Nkv, 32)) != ATTN_OK) return st;
+  if ((st = make_map(&tk, kv, d_qk, Nkv, planes, rs, rs * Nkv, decode_key_tile())) != ATTN_OK) return st;
   // Every slot the combine kernel reads is written first by the decode
   // kernel in the same call, so nothing needs clearing between calls.
   p.o_part = scratch;

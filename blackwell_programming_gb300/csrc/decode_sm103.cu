@@ -22,9 +22,10 @@
 // kernel then merges the partials of each row:
 //   LSE = log sum_s exp(lse_s),   O = sum_s exp(lse_s - LSE) O_s.
 //
-// Roles: warp 5 = TMA producer (Q once per segment, K tiles through a ring),
-// warp 4 = tcgen05 MMA issuer, warps 0-3 = softmax (one row per thread),
-// O rescale and epilogue.
+// Roles: warp 5 = TMA producer (the shared-memory part of Q once per
+// segment, K tiles through two rings), warp 4 = tcgen05 MMA issuer (whole
+// warp, one elected lane per instruction), warps 0-3 = the TMEM part of Q,
+// softmax (one row per thread), O rescale and epilogue.
 #include <cmath>
 
 #include "internal.h"
@@ -36,9 +37,14 @@ namespace {
 constexpr int DQK = 576;
 constexpr int DVH = 256;              // O columns per work item (half of d_v)
 constexpr int BM = 128;               // rows = query heads of one KV head
-constexpr int BN = 32;                // keys per K tile
+constexpr int BN = 64;                // keys per K tile
 constexpr int QCH = DQK / 64;         // 9 chunks of 64 features (128 bytes)
-constexpr int KS = 2;                 // K stages
+constexpr int Q_TMEM_FEATS = 384;     // Q features 0..383 live in TMEM, 384..575 in shared memory
+constexpr int Q_SMEM_CH = (DQK - Q_TMEM_FEATS) / 64;   // 3 chunks
+constexpr int A_CH = 5;               // K chunks outside this item's value half
+constexpr int B_CH = 4;               // K chunks of this item's value half (= V)
+constexpr int AS = 2;                 // ring A stages (released after Q K^T)
+constexpr int BS = 3;                 // ring B stages (released after P V)
 constexpr int kThreads = 192;
 constexpr int kMmaWarp = 4;
 constexpr int kTmaWarp = 5;
@@ -46,21 +52,26 @@ constexpr float kRescaleThreshold = 8.0f;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 constexpr uint32_t CHUNK_Q = BM * 128;              // 16 KB
-constexpr uint32_t CHUNK_K = BN * 128;              // 4 KB
-constexpr uint32_t Q_BYTES = QCH * CHUNK_Q;         // 147456
-constexpr uint32_t K_BYTES = QCH * CHUNK_K;         // 36864
+constexpr uint32_t CHUNK_K = BN * 128;              // 8 KB
+constexpr uint32_t QS_BYTES = Q_SMEM_CH * CHUNK_Q;  // 48 KB
+constexpr uint32_t A_BYTES = A_CH * CHUNK_K;        // 40 KB
+constexpr uint32_t B_BYTES = B_CH * CHUNK_K;        // 32 KB
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-constexpr uint32_t OFF_BAR = OFF_K + KS * K_BYTES;
-constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_KEMPTY = 2 + KS, B_SFULL = 2 + 2 * KS,
-              B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 1, B_OFULL = B_PVDONE + 1, B_OEMPTY = B_OFULL + 1,
-              B_DRAIN = B_OEMPTY + 1, NUM_BARS = B_DRAIN + 1;
+constexpr uint32_t OFF_A = OFF_Q + QS_BYTES;
+constexpr uint32_t OFF_B = OFF_A + AS * A_BYTES;
+constexpr uint32_t OFF_BAR = OFF_B + BS * B_BYTES;
+constexpr int B_QFULL = 0, B_QEMPTY = 1, B_QTFULL = 2, B_AFULL = 3, B_AEMPTY = B_AFULL + AS, B_BFULL = B_AEMPTY + AS,
+              B_BEMPTY = B_BFULL + BS, B_SFULL = B_BEMPTY + BS, B_PFULL = B_SFULL + 1, B_OFULL = B_PFULL + 1,
+              B_OEMPTY = B_OFULL + 1, B_DRAIN = B_OEMPTY + 1, NUM_BARS = B_DRAIN + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr uint32_t COL_S0 = 0;        // S buffers at columns 0 and 32
-constexpr uint32_t COL_O = 256;
+// TMEM: O half [0,256), S [256,320) (P as bf16 pairs in its first 32
+// columns), Q features 0..383 as bf16 pairs [320,512).
+constexpr uint32_t COL_O = 0;
+constexpr uint32_t COL_S = 256;
+constexpr uint32_t COL_Q = 320;
 constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, DVH, false, true);
 
@@ -107,13 +118,27 @@ struct SegmentWalker {
   }
 };
 
+// K chunk c (features 64c .. 64c+63) of a tile lives in ring B when it belongs
+// to the item's value half (chunks 4*half .. 4*half+3), else in ring A.
+__device__ __forceinline__ bool in_ring_b(int c, int half) { return c >= 4 * half && c < 4 * half + 4; }
+__device__ __forceinline__ int a_index(int c, int half) { return c < 4 * half ? c : c - 4; }
+
+// Why this layout: an MMA whose A operand comes from shared memory pays
+// about 32 cycles for the A read whatever N is, so a 64-key score tile
+// (N = 64) runs at two thirds of the tensor rate with A in shared memory and
+// at full rate with A in TMEM.  Two thirds of Q therefore sits in TMEM.
+// The 576-feature K tile is split into the five chunks the item needs only
+// for Q K^T (ring A, freed as soon as S is computed) and the four chunks that
+// are also its V half (ring B, freed after P V), so the shared memory left
+// beside Q's last third holds enough tiles in flight to cover the memory
+// latency.
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + OFF_Q, sK = sbase + OFF_K;
+  const uint32_t sQ = sbase + OFF_Q, sA = sbase + OFF_A, sB = sbase + OFF_B;
   auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC + 4);
@@ -124,14 +149,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0u;
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QEMPTY), 1);
-    for (int s = 0; s < KS; ++s) {
-      mbar_init(bar(B_KFULL + s), 1);
-      mbar_init(bar(B_KEMPTY + s), 1);
+    mbar_init(bar(B_QTFULL), 4);
+    for (int s = 0; s < AS; ++s) {
+      mbar_init(bar(B_AFULL + s), 1);
+      mbar_init(bar(B_AEMPTY + s), 1);
     }
-    mbar_init(bar(B_SFULL + 0), 1);
-    mbar_init(bar(B_SFULL + 1), 1);
+    for (int s = 0; s < BS; ++s) {
+      mbar_init(bar(B_BFULL + s), 1);
+      mbar_init(bar(B_BEMPTY + s), 1);
+    }
+    mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_PFULL), 4);
-    mbar_init(bar(B_PVDONE), 1);
     mbar_init(bar(B_OFULL), 1);
     mbar_init(bar(B_OEMPTY), 4);
     mbar_init(bar(B_DRAIN), 1);
@@ -153,118 +181,165 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       const uint64_t pol_k = l2_policy_evict_first();   // each K tile is read by the two halves, then dead
       const uint64_t pol_q = l2_policy_evict_last();
-      int ks = 0;
-      uint32_t kph = 0, qph = 0;
-      int k_last[KS], q_last = -1;
-      for (int s = 0; s < KS; ++s) k_last[s] = -1;
+      int as = 0, bs = 0;
+      uint32_t aph = 0, bph = 0, qph = 0;
+      // buffers filled (bit) and the parity of their last fill, for the drain
+      uint32_t filled = 0u, fill_par = 0u;
+      auto note_fill = [&](int b, uint32_t par) {
+        filled |= 1u << b;
+        fill_par = (fill_par & ~(1u << b)) | (par << b);
+      };
       SegmentWalker walk(p);
       Segment S;
       bool ok = true;
       while (ok && walk.next(S)) {
         if (!(ok = mbar_wait(bar(B_QEMPTY), qph ^ 1u, wctx))) break;
         qph ^= 1u;
-        mbar_arrive_expect_tx(bar(B_QFULL), Q_BYTES);
-        q_last = static_cast<int>(qph ^ 1u);
-        for (int kc = 0; kc < QCH; ++kc)
-          tma_load_3d(sQ + kc * CHUNK_Q, &tmQ, bar(B_QFULL), kc * 64, 0, S.plane, pol_q);
+        mbar_arrive_expect_tx(bar(B_QFULL), QS_BYTES);
+        note_fill(0, qph ^ 1u);
+        for (int c = 0; c < Q_SMEM_CH; ++c)
+          tma_load_3d(sQ + c * CHUNK_Q, &tmQ, bar(B_QFULL), Q_TMEM_FEATS + c * 64, 0, S.plane, pol_q);
         for (int j = 0; j < S.n; ++j) {
-          if (!(ok = mbar_wait(bar(B_KEMPTY + ks), kph ^ 1u, wctx))) break;
-          mbar_arrive_expect_tx(bar(B_KFULL + ks), K_BYTES);
-          k_last[ks] = static_cast<int>(kph);
-          for (int kc = 0; kc < QCH; ++kc)
-            tma_load_3d(sK + ks * K_BYTES + kc * CHUNK_K, &tmK, bar(B_KFULL + ks), kc * 64, (S.t0 + j) * BN,
-                        S.plane, pol_k);
-          if (++ks == KS) { ks = 0; kph ^= 1u; }
+          const int y = (S.t0 + j) * BN;
+          if (!(ok = mbar_wait(bar(B_AEMPTY + as), aph ^ 1u, wctx))) break;
+          mbar_arrive_expect_tx(bar(B_AFULL + as), A_BYTES);
+          note_fill(1 + as, aph);
+          for (int c = 0; c < QCH; ++c)
+            if (!in_ring_b(c, S.half))
+              tma_load_3d(sA + as * A_BYTES + a_index(c, S.half) * CHUNK_K, &tmK, bar(B_AFULL + as), c * 64, y,
+                          S.plane, pol_k);
+          if (++as == AS) { as = 0; aph ^= 1u; }
+          if (!(ok = mbar_wait(bar(B_BEMPTY + bs), bph ^ 1u, wctx))) break;
+          mbar_arrive_expect_tx(bar(B_BFULL + bs), B_BYTES);
+          note_fill(1 + AS + bs, bph);
+          for (int c = 0; c < B_CH; ++c)
+            tma_load_3d(sB + bs * B_BYTES + c * CHUNK_K, &tmK, bar(B_BFULL + bs), (4 * S.half + c) * 64, y, S.plane,
+                        pol_k);
+          if (++bs == BS) { bs = 0; bph ^= 1u; }
         }
       }
-      if (q_last >= 0) mbar_wait_drain(bar(B_QFULL), static_cast<uint32_t>(q_last));
-      for (int s = 0; s < KS; ++s)
-        if (k_last[s] >= 0) mbar_wait_drain(bar(B_KFULL + s), static_cast<uint32_t>(k_last[s]));
+      // Every issued copy must have landed before the CTA may exit.
+      for (int b = 0; b < 1 + AS + BS; ++b) {
+        if (!((filled >> b) & 1u)) continue;
+        const int full = b == 0 ? B_QFULL : (b < 1 + AS ? B_AFULL + (b - 1) : B_BFULL + (b - 1 - AS));
+        mbar_wait_drain(bar(full), (fill_par >> b) & 1u);
+      }
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      int ks = 0, prev = 0;
-      uint32_t kph = 0, qph = 0, pph = 0, oeph = 0;
-      SegmentWalker walk(p);
-      Segment S;
-      bool ok = true;
-      while (ok && walk.next(S)) {
-        if (!(ok = mbar_wait(bar(B_OEMPTY), oeph ^ 1u, wctx))) break;
-        oeph ^= 1u;
-        if (!(ok = mbar_wait(bar(B_QFULL), qph, wctx))) break;
-        qph ^= 1u;
-        tc_fence_after();
-        for (int j = 0; j <= S.n; ++j) {
-          if (j < S.n) {
-            if (!(ok = mbar_wait(bar(B_KFULL + ks), kph, wctx))) break;
-            tc_fence_after();
-            const uint32_t kbase = sK + ks * K_BYTES;
-            const uint32_t dS = tm + COL_S0 + (j & 1) * BN;
-#pragma unroll 4
-            for (int kk = 0; kk < DQK / 16; ++kk) {
-              const uint32_t off = (kk & 3) * 32;
-              mma_ss(dS, smem_desc_sw128(sQ + (kk >> 2) * CHUNK_Q + off, 16, 1024),
-                     smem_desc_sw128(kbase + (kk >> 2) * CHUNK_K + off, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(bar(B_SFULL + (j & 1)));
-            if (j == S.n - 1) mma_commit(bar(B_QEMPTY));
-          }
-          if (j >= 1) {
-            if (!(ok = mbar_wait(bar(B_PFULL), pph, wctx))) break;
-            pph ^= 1u;
-            tc_fence_after();
-            // V half = K features [256 * half, 256 * half + 256): chunks 4*half .. 4*half+3
-            const uint32_t vbase = sK + prev * K_BYTES + (4 * S.half) * CHUNK_K;
-            const uint32_t aP = tm + COL_S0 + ((j - 1) & 1) * BN;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ts(tm + COL_O, aP + kk * 8, smem_desc_sw128(vbase + kk * 16 * 128, CHUNK_K, 1024), IDESC_PV,
-                     (j - 1 > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(bar(B_PVDONE));
-            mma_commit(bar(B_KEMPTY + prev));
-          }
-          if (j < S.n) {
-            prev = ks;
-            if (++ks == KS) { ks = 0; kph ^= 1u; }
-          } else {
-            mma_commit(bar(B_OFULL));
-          }
-        }
-      }
-      mma_commit(bar(B_DRAIN));
-      mbar_wait_drain(bar(B_DRAIN), 0);
-    }
-    __syncwarp();
-  } else if (warp < 4) {
-    // ------------------------------------------- softmax, rescale, epilogue
-    const int r = static_cast<int>(warp * 32 + lane);
-    const uint32_t lane_addr = (warp * 32u) << 16;
-    const float sl2 = p.scale_log2;
-    uint32_t sph[2] = {0, 0}, pvph = 0, ofph = 0;
+    // ------------------------------------------------ MMA issuer (whole warp)
+    int as = 0, bs = 0;
+    uint32_t aph = 0, bph = 0, qph = 0, qtph = 0, pph = 0, oeph = 0;
+    const uint64_t qs_desc = smem_desc_sw128(sQ, 16, 1024);
+    const uint64_t a_desc0 = smem_desc_sw128(sA, 16, 1024);
+    const uint64_t b_desc0 = smem_desc_sw128(sB, 16, 1024);
+    const uint64_t v_desc0 = smem_desc_sw128(sB, CHUNK_K, 1024);
+    const uint32_t dS = tm + COL_S, dO = tm + COL_O, aQ = tm + COL_Q;
     SegmentWalker walk(p);
     Segment S;
     bool ok = true;
     while (ok && walk.next(S)) {
+      if (!(ok = warp_wait(bar(B_OEMPTY), oeph ^ 1u, wctx))) break;
+      oeph ^= 1u;
+      if (!(ok = warp_wait(bar(B_QFULL), qph, wctx))) break;
+      qph ^= 1u;
+      if (!(ok = warp_wait(bar(B_QTFULL), qtph, wctx))) break;
+      qtph ^= 1u;
+      tc_fence_after();
+      for (int j = 0; j < S.n && ok; ++j) {
+        if (!(ok = warp_wait(bar(B_AFULL + as), aph, wctx))) break;
+        if (!(ok = warp_wait(bar(B_BFULL + bs), bph, wctx))) break;
+        // S = Q K^T over 36 K steps of 16 features
+        const uint64_t ad = a_desc0 + ((as * A_BYTES) >> 4);
+        const uint64_t bd = b_desc0 + ((bs * B_BYTES) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < DQK / 16; ++kk) {
+          const int c = kk >> 2;
+          const uint32_t in_chunk = ((kk & 3) * 32) >> 4;
+          const uint64_t kdesc = in_ring_b(c, S.half) ? bd + (((c - 4 * S.half) * CHUNK_K) >> 4) + in_chunk
+                                                        : ad + ((a_index(c, S.half) * CHUNK_K) >> 4) + in_chunk;
+          if (kk < Q_TMEM_FEATS / 16) {
+            mma_ts_warp(dS, aQ + kk * 8, kdesc, IDESC_S, kk > 0 ? 1u : 0u);
+          } else {
+            const uint64_t qd = qs_desc + (((c - Q_TMEM_FEATS / 64) * CHUNK_Q) >> 4) + in_chunk;
+            mma_ss_warp(dS, qd, kdesc, IDESC_S, 1u);
+          }
+        }
+        mma_commit_warp(bar(B_SFULL));
+        mma_commit_warp(bar(B_AEMPTY + as));
+        if (++as == AS) { as = 0; aph ^= 1u; }
+        if (j == S.n - 1) mma_commit_warp(bar(B_QEMPTY));
+        // O += P V: P (64 keys, bf16 pairs) from TMEM over S, V = ring B
+        if (!(ok = warp_wait(bar(B_PFULL), pph, wctx))) break;
+        pph ^= 1u;
+        tc_fence_after();
+        const uint64_t vd = v_desc0 + ((bs * B_BYTES) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts_warp(dO, dS + kk * 8, vd + ((kk * 16 * 128) >> 4), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_warp(bar(B_BEMPTY + bs));
+        if (++bs == BS) { bs = 0; bph ^= 1u; }
+      }
+      if (!ok) break;
+      mma_commit_warp(bar(B_OFULL));
+    }
+    mma_commit_warp(bar(B_DRAIN));
+    mbar_wait_drain(bar(B_DRAIN), 0);
+    __syncwarp();
+  } else if (warp < 4) {
+    // ----------------------------- Q into TMEM, softmax, rescale, epilogue
+    const int r = static_cast<int>(warp * 32 + lane);
+    const bool live = r < p.group;
+    const uint32_t lane_addr = (warp * 32u) << 16;
+    const float sl2 = p.scale_log2;
+    const uint64_t c2 = f2_pack(sl2, sl2);
+    uint32_t sph = 0, ofph = 0, qeph = 0;
+    SegmentWalker walk(p);
+    Segment S;
+    bool ok = true;
+    while (ok && walk.next(S)) {
+      // Q features 0..383 of this head into TMEM (bf16 pairs, column c = features
+      // 2c, 2c+1) once the previous segment's last Q K^T has finished.
+      if (!(ok = warp_wait(bar(B_QEMPTY), qeph ^ 1u, wctx))) break;
+      qeph ^= 1u;
+      tc_fence_after();
+      {
+        const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(S.plane) * p.group + (live ? r : 0)) * DQK);
+#pragma unroll 1
+        for (int c = 0; c < Q_TMEM_FEATS / 64; ++c) {
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 x = live ? qrow[c * 8 + i] : make_uint4(0u, 0u, 0u, 0u);
+            w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
+          }
+          tmem_st32u(tm + lane_addr + COL_Q + c * 32, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_QTFULL));
+      }
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < S.n; ++j) {
-        const int sb = j & 1;
-        if (!(ok = warp_wait(bar(B_SFULL + sb), sph[sb], wctx))) break;
-        sph[sb] ^= 1u;
+        if (!(ok = warp_wait(bar(B_SFULL), sph, wctx))) break;
+        sph ^= 1u;
         tc_fence_after();
-        float v[32];
-        tmem_ld32(tm + lane_addr + COL_S0 + sb * BN, v);
+        float v[BN];
+        tmem_ld64(tm + lane_addr + COL_S, v);
         const int key0 = (S.t0 + j) * BN;
         const bool ragged = key0 + BN > p.Nkv;
         if (ragged) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < BN; ++i)
             if (key0 + i >= p.Nkv) v[i] = -INFINITY;
         }
-        float mx = -INFINITY;
+        float mx8[8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[i]);
+        for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(v[2 * a], v[2 * a + 1]);
+#pragma unroll
+        for (int i = 8; i < BN / 2; ++i) mx8[i & 7] = fmax3(mx8[i & 7], v[2 * i], v[2 * i + 1]);
+        const float mx = fmaxf(fmax3(fmax3(mx8[0], mx8[1], mx8[2]), mx8[3], mx8[4]), fmax3(mx8[5], mx8[6], mx8[7]));
         const float m_new = (mx == -INFINITY) ? -INFINITY : mx * sl2;
         float alpha = 1.f;
         const bool grow = m_new > m_used + kRescaleThreshold;
@@ -273,36 +348,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = m_new;
         }
         l *= alpha;
-        if (j >= 1) {
-          // O is only touched once the previous P.V has finished.
-          if (!(ok = warp_wait(bar(B_PVDONE), pvph, wctx))) break;
-          pvph ^= 1u;
-          tc_fence_after();
-          if (__any_sync(kFull, grow)) {
+        // O is stable here: this tile's S was issued after the previous P V.
+        if (j >= 1 && __any_sync(kFull, grow)) {
 #pragma unroll 1
-            for (int c = 0; c < DVH / 32; ++c) {
-              float o[32];
-              tmem_ld32(tm + lane_addr + COL_O + c * 32, o);
+          for (int c = 0; c < DVH / 32; ++c) {
+            float o[32];
+            tmem_ld32(tm + lane_addr + COL_O + c * 32, o);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= alpha;
-              tmem_st32(tm + lane_addr + COL_O + c * 32, o);
-            }
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tm + lane_addr + COL_O + c * 32, o);
           }
         }
         const float base = (m_used == -INFINITY) ? 0.f : m_used;
-        uint32_t pk[16];
+        const uint64_t nb2 = f2_pack(-base, -base);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[BN / 2];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float p0 = ex2(fmaf(v[2 * i], sl2, -base));
-          float p1 = ex2(fmaf(v[2 * i + 1], sl2, -base));
+        for (int i = 0; i < BN / 2; ++i) {
+          const uint64_t x = f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), c2, nb2);
+          float p0 = ex2(f2_lo(x));
+          float p1 = ex2(f2_hi(x));
           if (ragged) {
             if (key0 + 2 * i >= p.Nkv) p0 = 0.f;
             if (key0 + 2 * i + 1 >= p.Nkv) p1 = 0.f;
           }
-          l += p0 + p1;
+          acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tm + lane_addr + COL_S0 + sb * BN, pk);
+        tmem_st32u(tm + lane_addr + COL_S, pk);
+        const uint64_t a01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+        l += f2_lo(a01) + f2_hi(a01);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -311,23 +386,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (!(ok = warp_wait(bar(B_OFULL), ofph, wctx))) break;
       ofph ^= 1u;
-      // the last P.V of the segment also completed pv_done once
-      if (!(ok = warp_wait(bar(B_PVDONE), pvph, wctx))) break;
-      pvph ^= 1u;
       tc_fence_after();
       const size_t slot = static_cast<size_t>(blockIdx.x) * p.max_seg + S.slot;
-      const bool live = r < p.group;
       float* orow = p.o_part + (slot * BM + r) * DVH;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll 1
       for (int c = 0; c < DVH / 32; ++c) {
-        float v[32];
-        tmem_ld32(tm + lane_addr + COL_O + c * 32, v);
+        float o[32];
+        tmem_ld32(tm + lane_addr + COL_O + c * 32, o);
         if (live) {
           float4* dst = reinterpret_cast<float4*>(orow + c * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(v[4 * i] * inv_l, v[4 * i + 1] * inv_l, v[4 * i + 2] * inv_l, v[4 * i + 3] * inv_l);
+            dst[i] = make_float4(o[4 * i] * inv_l, o[4 * i + 1] * inv_l, o[4 * i + 2] * inv_l, o[4 * i + 3] * inv_l);
         }
       }
       if (live) p.lse_part[slot * BM + r] = (l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
@@ -345,46 +416,83 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// One block per (half, plane); thread c owns O column half * 256 + c.  `grid`
-// is the decode kernel's grid size, which fixes where the partials are.
-__global__ void __launch_bounds__(DVH) combine_kernel(const DecodeParams p, int grid, float* o, float* lse) {
-  const int half = blockIdx.x / p.planes;
-  const int plane = blockIdx.x - half * p.planes;
-  const int c = threadIdx.x;
+// One warp per output row and value half: lanes read the row's partial LSEs
+// (32 at a time), reduce the maximum and the sum of weights with shuffles,
+// and each lane merges its 8 of the 256 columns with float4 loads.  `grid` is the decode kernel's grid
+// size, which fixes where the partials are.
+constexpr int kCombineWarps = 8;
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecodeParams p, int grid, float* o,
+                                                                     float* lse) {
+  const int wid = blockIdx.x * kCombineWarps + static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int rows = p.planes * p.group;
+  if (wid >= 2 * rows) return;
+  const int half = wid / rows;
+  const int rr = wid - half * rows;
+  const int plane = rr / p.group;
+  const int r = rr - plane * p.group;
   const long long tiles = p.tiles;
   const long long total = 2LL * p.planes * tiles;
   const long long sg = static_cast<long long>(half) * p.planes + plane;
   const long long gs = sg * tiles, ge = gs + tiles - 1;
   const int c_first = static_cast<int>(((gs + 1) * grid + total - 1) / total - 1);
   const int c_last = static_cast<int>(((ge + 1) * grid + total - 1) / total - 1);
-  for (int r = 0; r < p.group; ++r) {
-    float mx = -INFINITY;
-    for (int cta = c_first; cta <= c_last; ++cta) {
-      const long long b0 = range_begin(total, cta, grid), b1 = range_begin(total, cta + 1, grid);
-      if (b1 <= b0) continue;
-      const size_t slot = static_cast<size_t>(cta) * p.max_seg + static_cast<size_t>(sg - b0 / tiles);
-      mx = fmaxf(mx, p.lse_part[slot * BM + r]);
-    }
-    float acc = 0.f, tot = 0.f;
-    if (mx != -INFINITY) {
-      for (int cta = c_first; cta <= c_last; ++cta) {
-        const long long b0 = range_begin(total, cta, grid), b1 = range_begin(total, cta + 1, grid);
-        if (b1 <= b0) continue;
-        const size_t slot = static_cast<size_t>(cta) * p.max_seg + static_cast<size_t>(sg - b0 / tiles);
-        const float w = expf(p.lse_part[slot * BM + r] - mx);
-        tot += w;
-        acc += w * p.o_part[(slot * BM + r) * DVH + c];
+  const int count = c_last - c_first + 1;   // CTAs whose range meets this segment
+  // Partial i (0 <= i < count) belongs to CTA c_first + i; lanes take them
+  // 32 at a time.
+  auto partial = [&](int i, size_t& slot) -> float {
+    const int cta = c_first + i;
+    const long long b0 = range_begin(total, cta, grid), b1 = range_begin(total, cta + 1, grid);
+    if (b1 <= b0) return -INFINITY;
+    slot = static_cast<size_t>(cta) * p.max_seg + static_cast<size_t>(sg - b0 / tiles);
+    return p.lse_part[slot * BM + r];
+  };
+  float mx = -INFINITY;
+  for (int base = 0; base < count; base += 32) {
+    size_t slot = 0;
+    if (base + lane < count) mx = fmaxf(mx, partial(base + lane, slot));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+  float tot = 0.f;
+  float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
+  if (mx != -INFINITY) {
+    for (int base = 0; base < count; base += 32) {
+      size_t my_slot = 0;
+      float w = 0.f;
+      if (base + lane < count) {
+        const float l = partial(base + lane, my_slot);
+        w = (l == -INFINITY) ? 0.f : expf(l - mx);
+      }
+      tot += w;
+      const int m = min(32, count - base);
+      for (int i = 0; i < m; ++i) {
+        const float wi = __shfl_sync(kFull, w, i);
+        const unsigned long long si = __shfl_sync(kFull, static_cast<unsigned long long>(my_slot), i);
+        if (wi == 0.f) continue;
+        const float4* src =
+            reinterpret_cast<const float4*>(p.o_part + (static_cast<size_t>(si) * BM + r) * DVH) + lane * 2;
+        const float4 x = src[0], y = src[1];
+        acc0.x += wi * x.x; acc0.y += wi * x.y; acc0.z += wi * x.z; acc0.w += wi * x.w;
+        acc1.x += wi * y.x; acc1.y += wi * y.y; acc1.z += wi * y.z; acc1.w += wi * y.w;
       }
     }
-    const size_t row = static_cast<size_t>(plane) * p.group + r;
-    o[row * (2 * DVH) + half * DVH + c] = (tot > 0.f) ? acc / tot : 0.f;
-    if (half == 0 && c == 0 && lse != nullptr) lse[row] = (tot > 0.f) ? mx + logf(tot) : -INFINITY;
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(kFull, tot, off);
+  const float inv = (tot > 0.f) ? 1.f / tot : 0.f;
+  acc0.x *= inv; acc0.y *= inv; acc0.z *= inv; acc0.w *= inv;
+  acc1.x *= inv; acc1.y *= inv; acc1.z *= inv; acc1.w *= inv;
+  float4* dst = reinterpret_cast<float4*>(o + static_cast<size_t>(rr) * (2 * DVH) + half * DVH) + lane * 2;
+  dst[0] = acc0;
+  dst[1] = acc1;
+  if (half == 0 && lane == 0 && lse != nullptr) lse[rr] = (tot > 0.f) ? mx + logf(tot) : -INFINITY;
 }
 
 }  // namespace
 
 int decode_tiles(int Nkv) { return (Nkv + BN - 1) / BN; }
+int decode_key_tile() { return BN; }
 
 int decode_max_segments(int planes, int tiles, int grid) {
   const long long total = 2LL * planes * tiles;
@@ -408,7 +516,8 @@ cudaError_t launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const De
 }
 
 cudaError_t launch_combine(const DecodeParams& p, int grid, float* o, float* lse, cudaStream_t stream) {
-  combine_kernel<<<2 * p.planes, DVH, 0, stream>>>(p, grid, o, lse);
+  const int warps = 2 * p.planes * p.group;
+  combine_kernel<<<(warps + kCombineWarps - 1) / kCombineWarps, kCombineWarps * 32, 0, stream>>>(p, grid, o, lse);
   return cudaGetLastError();
 }
 

@@ -29,12 +29,13 @@ cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, 
 // features of K).  The Hq / Hkv query heads that share a KV head form the
 // rows of one 128-row tile; a "plane" is one (batch, KV head) pair.
 struct DecodeParams {
+  const uint16_t* q;   // bf16 Q [planes * group, 576] (the kernel loads part of it into TMEM)
   float* o_part;       // [grid * max_seg, 128, 256] partial O (normalised), per half
   float* lse_part;     // [grid * max_seg, 128] partial LSE (natural log)
   int planes;          // B * Hkv
   int group;           // Hq / Hkv, <= 128
   int Nkv;
-  int tiles;           // ceil(Nkv / 32)
+  int tiles;           // ceil(Nkv / decode_key_tile())
   int max_seg;         // partial slots per CTA
   float scale_log2;    // scale * log2(e)
   unsigned* err;
@@ -43,6 +44,7 @@ struct DecodeParams {
 // Number of partial slots each CTA needs for a grid of `grid` CTAs.
 int decode_max_segments(int planes, int tiles, int grid);
 int decode_tiles(int Nkv);
+int decode_key_tile();   // keys per K tile of the decode kernel (TMA box rows)
 
 cudaError_t launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const DecodeParams& p, int grid,
                           cudaStream_t stream);
