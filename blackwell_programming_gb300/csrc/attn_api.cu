@@ -17,7 +17,7 @@
 
 #include <cudaTypedefs.h>
 
-#include "../../include/gbattn.h"
+#include "gbattn.h"
 #include "internal.h"
 
 namespace gbattn {
