@@ -24,13 +24,9 @@
 //    MMA computes O_t += P_t V_j with P read straight from TMEM.  The two query tiles ping-pong: the tensor core
 //    works on one tile while the softmax warpgroup of the other one runs.
 //  * Warpgroups 0 and 1 own query tile 0 and 1.  TMEM lane i is row i, so a
-//    thread owns a whole row: max, exp2 and sum stay in-thread.  The
-//    exponentials use the running maximum of the earlier tiles, so P, the
-//    row sum and the tile's maximum come out of one pass.  When a tile's
-//    maximum exceeds that reference by more than 2^8, the next tile moves
-//    the reference and rescales O (P and l always share one reference, so
-//    the result stays exact); only a jump past 2^64 redoes the pass.  The
-//    same warps run the epilogue.
+//    thread owns a whole row: max, exp2 and sum stay in-thread.  They also
+//    rescale O (only when the running max grew by more than 2^8, which keeps
+//    the result exact) and run the epilogue: O / l and LSE to global memory.
 //
 // TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D).
 #include <cmath>
@@ -47,8 +43,7 @@ constexpr int kThreads = 384;         // 3 warpgroups
 constexpr int kMmaWarp0 = 8;    // MMA issuer for query tile 0 (also owns the TMEM allocation)
 constexpr int kTmaWarp = 9;
 constexpr int kMmaWarp1 = 10;   // MMA issuer for query tile 1
-constexpr float kRescaleThreshold = 8.0f;   // log2 units: move the reference past 2^8 ...
-constexpr float kRedoThreshold = 64.0f;     // ... and redo a tile's pass only past 2^64
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only past 2^8
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 // Register split: the MMA / TMA warpgroup gives registers to the two softmax
 // warpgroups.  128 * 96 + 256 * 200 = 63488 must not exceed the launch
@@ -112,45 +107,6 @@ __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p) {
   U.n[0] = kv_tiles_for(U.qb * 2 * BM, p);
   U.n[1] = kv_tiles_for(U.qb * 2 * BM + BM, p);
   return U;
-}
-
-// Maximum of a 128-score row (masked scores are -inf).
-__device__ __forceinline__ float row_max(const float (&v)[BN]) {
-  float mx8[8];
-#pragma unroll
-  for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(v[2 * a], v[2 * a + 1]);
-#pragma unroll
-  for (int i = 8; i < BN / 2; ++i) mx8[i & 7] = fmax3(mx8[i & 7], v[2 * i], v[2 * i + 1]);
-  return fmaxf(fmax3(fmax3(mx8[0], mx8[1], mx8[2]), mx8[3], mx8[4]), fmax3(mx8[5], mx8[6], mx8[7]));
-}
-
-// One pass over a 128-score row (masked scores are -inf): p = 2^(s * c -
-// base) packed as bf16 pairs, their sum, and the row maximum.  Argument with
-// paired FMAs, exponential on the SFU (2^-inf = 0 for masked scores when
-// c > 0; with c = 0 every visible score weighs the same and masked ones are
-// zeroed explicitly), sum in four paired accumulators, maximum in eight
-// three-input chains.
-__device__ __forceinline__ void exp_row(const float (&v)[BN], uint64_t c2, float base, uint32_t (&pk)[BN / 2],
-                                        float& psum, float& mx) {
-  const uint64_t nb2 = f2_pack(-base, -base);
-  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-  float mx8[8];
-#pragma unroll
-  for (int a = 0; a < 8; ++a) mx8[a] = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < BN / 2; ++i) {
-    mx8[i & 7] = fmax3(mx8[i & 7], v[2 * i], v[2 * i + 1]);
-    const uint64_t x = f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), c2, nb2);
-    float p0 = ex2(f2_lo(x));
-    float p1 = ex2(f2_hi(x));
-    if (v[2 * i] == -INFINITY) p0 = 0.f;
-    if (v[2 * i + 1] == -INFINITY) p1 = 0.f;
-    acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-    pk[i] = pack_bf16x2(p0, p1);
-  }
-  const uint64_t a01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
-  psum = f2_lo(a01) + f2_hi(a01);
-  mx = fmaxf(fmax3(fmax3(mx8[0], mx8[1], mx8[2]), mx8[3], mx8[4]), fmax3(mx8[5], mx8[6], mx8[7]));
 }
 
 // Snake order over rounds of gridDim.x units.
@@ -389,7 +345,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tm + lane_addr + C::col_s(t);
     const uint32_t tO = tm + lane_addr + C::col_o(t);
     const float sl2 = p.scale_log2;
-    const uint64_t c2 = f2_pack(sl2, sl2);
     const int delta = p.Nkv - p.Nq;
     uint32_t sph = 0, ofph = 0;
     for (int it = 0;; ++it) {
@@ -399,9 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = U.n[t];
       const int q0 = (U.qb * 2 + t) * BM;
       const int row = q0 + row_in_tile;
-      // m_used: reference maximum of P and l (log2 units); m_next: the
-      // reference the next tile moves to.
-      float m_used = -INFINITY, m_next = -INFINITY, l = 0.f;
+      float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
         if (!(ok = warp_wait(bar(C::B_SFULL + t), sph, wctx))) break;
@@ -418,18 +371,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < BN; ++i)
             if (key0 + i > key_lim) v[i] = -INFINITY;
         }
-        if (j == 0) {
-          // First tile of the row block: its maximum sets the reference.
-          const float mx0 = row_max(v);
-          m_used = (mx0 == -INFINITY) ? -INFINITY : mx0 * sl2;
-          m_next = m_used;
-        } else if (__any_sync(kFull, m_next > m_used)) {
-          // An earlier tile's maximum grew past the threshold: move the
-          // reference now that O holds that tile's P V (this tile's S was
-          // issued after it), rescaling l and O by 2^(old - new).
-          const float alpha = (m_next > m_used) ? ex2(m_used - m_next) : 1.f;
-          m_used = fmaxf(m_used, m_next);
-          l *= alpha;
+        // Row maximum: eight independent three-input max chains, then merge.
+        float mx8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(v[2 * a], v[2 * a + 1]);
+#pragma unroll
+        for (int i = 8; i < BN / 2; ++i) mx8[i & 7] = fmax3(mx8[i & 7], v[2 * i], v[2 * i + 1]);
+        const float mx = fmaxf(fmax3(fmax3(mx8[0], mx8[1], mx8[2]), mx8[3], mx8[4]),
+                               fmax3(mx8[5], mx8[6], mx8[7]));
+        const float m_new = (mx == -INFINITY) ? -INFINITY : mx * sl2;
+        float alpha = 1.f;
+        const bool grow = m_new > m_used + kRescaleThreshold;
+        if (grow) {
+          alpha = ex2(m_used - m_new);
+          m_used = m_new;
+        }
+        l *= alpha;
+        if (j > 0 && __any_sync(kFull, grow)) {
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
@@ -439,47 +397,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tO + c * 32, o);
           }
         }
-        // One pass with the running reference maximum m_used gives P, the
-        // row sum and this tile's maximum together.  P and l share the
-        // reference, so a P above 1 is exact; a tile may exceed the
-        // reference by up to 2^64 (finite in fp32 sums and bf16 P) and then
-        // moves the reference for the next tile.
+        const float base = (m_used == -INFINITY) ? 0.f : m_used;
+        // P = 2^(s * scale * log2 e - m): the argument with paired FMAs, the
+        // exponential on the SFU, the row sum in four paired accumulators,
+        // P as bf16 pairs written over S.
+        const uint64_t c2 = f2_pack(sl2, sl2);
+        const uint64_t nb2 = f2_pack(-base, -base);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[BN / 2];
-        float psum, mx;
-        exp_row(v, c2, (m_used == -INFINITY) ? 0.f : m_used, pk, psum, mx);
-        const float m_new = (mx == -INFINITY) ? -INFINITY : mx * sl2;
-        if (m_new > m_used + kRescaleThreshold) m_next = fmaxf(m_next, m_new);
-        if (__any_sync(kFull, m_new > m_used + kRedoThreshold)) {
-          // Very rare: a jump past 2^64.  Rows that jumped move the reference
-          // at once (rescaling l and O) and the pass is redone from S, still
-          // intact in TMEM because P is not stored yet.
-          float alpha = 1.f;
-          if (m_new > m_used + kRedoThreshold) {
-            alpha = ex2(m_used - m_new);
-            m_used = m_new;
-          }
-          l *= alpha;
-          if (j > 0) {
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-              float o[32];
-              tmem_ld32(tO + c * 32, o);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= alpha;
-              tmem_st32(tO + c * 32, o);
-            }
-          }
-          tmem_ld128(tS, v);
+        for (int i = 0; i < BN / 2; ++i) {
+          const uint64_t x = f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), c2, nb2);
+          float p0 = ex2(f2_lo(x));
+          float p1 = ex2(f2_hi(x));
           if (need_mask) {
-#pragma unroll
-            for (int i = 0; i < BN; ++i)
-              if (key0 + i > key_lim) v[i] = -INFINITY;
+            if (key0 + 2 * i > key_lim) p0 = 0.f;
+            if (key0 + 2 * i + 1 > key_lim) p1 = 0.f;
           }
-          exp_row(v, c2, (m_used == -INFINITY) ? 0.f : m_used, pk, psum, mx);
-          m_next = fmaxf(m_next, m_used);
+          acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st64(tS, pk);   // P over the first 64 columns of S
-        l += psum;
+        tmem_st64(tS, pk);
+        const uint64_t a01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
+        l += f2_lo(a01) + f2_hi(a01);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
