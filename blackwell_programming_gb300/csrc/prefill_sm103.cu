@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_kv = l2_policy_evict_last();
       const uint64_t pol_q = l2_policy_evict_first();
       int ks = 0, vs = 0;
-      uint32_t kph = 0, vph = 0, qph[2] = {0, 0};
+      uint32_t kph = 0, vph = 0, qph = 0u;   // bit t: parity of Q tile t
       // Buffers filled so far (bit b) and the parity of their last fill, for
       // the drain at exit.  Bits: Q tile t -> t, K stage s -> 2 + s,
       // V stage s -> 2 + KS + s.
@@ -195,10 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int t = 0; t < 2 && ok; ++t) {
           if (U.n[t] == 0) continue;
-          if (!(ok = mbar_wait(bar(C::B_QEMPTY + t), qph[t] ^ 1u, wctx))) break;
-          qph[t] ^= 1u;
+          if (!(ok = mbar_wait(bar(C::B_QEMPTY + t), ((qph >> t) & 1u) ^ 1u, wctx))) break;
+          qph ^= 1u << t;
           mbar_arrive_expect_tx(bar(C::B_QFULL + t), C::Q_BYTES);
-          note_fill(t, qph[t] ^ 1u);
+          note_fill(t, ((qph >> t) & 1u) ^ 1u);
           for (int kc = 0; kc < C::KCH; ++kc)
             tma_load_3d(sQ + t * C::Q_BYTES + kc * C::CHUNK_Q, &tmQ, bar(C::B_QFULL + t), kc * 64,
                         (U.qb * 2 + t) * BM, U.b * p.Hq + U.h, pol_q);
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = unit_at(it);
         if (u >= p.num_units) break;
         const Unit U = decode_unit(u, p);
-        const int n = U.n[t];
+        const int n = t ? U.n[1] : U.n[0];
         const int nmax = max(U.n[0], U.n[1]);
         bool o_waited = false;
         bool ok = true;
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = unit_at(it);
       if (u >= p.num_units) break;
       const Unit U = decode_unit(u, p);
-      const int n = U.n[t];
+      const int n = t ? U.n[1] : U.n[0];
       const int q0 = (U.qb * 2 + t) * BM;
       const int row = q0 + row_in_tile;
       float m_used = -INFINITY, l = 0.f;
@@ -400,20 +400,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float base = (m_used == -INFINITY) ? 0.f : m_used;
         // P = 2^(s * scale * log2 e - m): the argument with paired FMAs, the
         // exponential on the SFU, the row sum in four paired accumulators,
-        // P as bf16 pairs written over S.
-        const uint64_t c2 = f2_pack(sl2, sl2);
+        // P as bf16 pairs written over S.  Masked keys need no second test
+        // here: their logit is -inf and ex2(-inf) = 0.  The one exception is
+        // scale 0 (0 * -inf): then the visible logits become 0 with a unit
+        // factor.  The loop itself carries no mask code, so the compiler
+        // emits nothing per element for it.
+        float csl = sl2;
+        if (need_mask && sl2 == 0.f) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i) v[i] = (v[i] == -INFINITY) ? -INFINITY : 0.f;
+          csl = 1.f;
+        }
+        const uint64_t c2 = f2_pack(csl, csl);
         const uint64_t nb2 = f2_pack(-base, -base);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[BN / 2];
 #pragma unroll
         for (int i = 0; i < BN / 2; ++i) {
           const uint64_t x = f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), c2, nb2);
-          float p0 = ex2(f2_lo(x));
-          float p1 = ex2(f2_hi(x));
-          if (need_mask) {
-            if (key0 + 2 * i > key_lim) p0 = 0.f;
-            if (key0 + 2 * i + 1 > key_lim) p1 = 0.f;
-          }
+          const float p0 = ex2(f2_lo(x));
+          const float p1 = ex2(f2_hi(x));
           acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }

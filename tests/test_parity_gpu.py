@@ -50,6 +50,9 @@ SMALL = [
     W("noncausal_many_tiles_d128", B=1, Hq=4, Hkv=4, Nq=384, Nkv=1000, d_qk=128, d_v=128, causal=False,
       scale=0.088, q_factor=4.0),
     W("zero_scale_d64", B=1, Hq=1, Hkv=1, Nq=256, Nkv=384, d_qk=64, d_v=64, causal=False, scale=0.0),
+    # scale 0 under a causal mask: the masked logits must stay excluded (0 * -inf)
+    W("zero_scale_causal_d128", B=1, Hq=2, Hkv=1, Nq=300, Nkv=257, d_qk=128, d_v=128, causal=True, scale=0.0),
+    W("zero_scale_causal_d64", B=1, Hq=1, Hkv=1, Nq=200, Nkv=200, d_qk=64, d_v=64, causal=True, scale=0.0),
     W("decode_small", B=2, Hq=16, Hkv=1, Nq=1, Nkv=300, d_qk=576, d_v=512, causal=False,
       scale=1 / math.sqrt(192), v_aliases_k=True),
     W("decode_two_kv_heads", B=3, Hq=64, Hkv=2, Nq=1, Nkv=1111, d_qk=576, d_v=512, causal=True,
