@@ -43,6 +43,12 @@ struct DeviceInfo {
   int status = ATTN_OK;
   int num_sms = 0;
   unsigned* err = nullptr;
+  // Stream-ordered pool for the split-KV workspace.  Its release threshold
+  // is unlimited, so memory freed at the end of one call is reused by the
+  // next instead of being unmapped at every synchronisation and mapped again
+  // (which the default pool does, at about 0.1 ms per call for a 40 MB
+  // workspace).
+  cudaMemPool_t pool = nullptr;
 };
 
 std::mutex g_mu;
@@ -72,6 +78,15 @@ int device_info(DeviceInfo** out) {
     void* p = nullptr;
     if ((e = cudaGetSymbolAddress(&p, g_device_error)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
     d.err = static_cast<unsigned*>(p);
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if ((e = cudaMemPoolCreate(&d.pool, &props)) != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+    uint64_t keep = UINT64_MAX;
+    if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemPoolSetAttribute");
     if (g_encode == nullptr) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -251,8 +266,8 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, 
     p.max_seg = decode_max_segments(planes, p.tiles, grid);
     const size_t n_slots = static_cast<size_t>(grid) * p.max_seg * 128;
     void* ws = nullptr;
-    if ((e = cudaMallocAsync(&ws, n_slots * (256 + 1) * sizeof(float), stream)) != cudaSuccess)
-      return cuda_fail(e, "cudaMallocAsync(decode workspace)");
+    if ((e = cudaMallocFromPoolAsync(&ws, n_slots * (256 + 1) * sizeof(float), dev->pool, stream)) != cudaSuccess)
+      return cuda_fail(e, "cudaMallocFromPoolAsync(decode workspace)");
     p.o_part = static_cast<float*>(ws);
     p.lse_part = p.o_part + n_slots * 256;
     if ((e = launch_decode(tq, tk, p, grid, stream)) != cudaSuccess) {

@@ -292,7 +292,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool live = r < p.group;
     const uint32_t lane_addr = (warp * 32u) << 16;
     const float sl2 = p.scale_log2;
-    const uint64_t c2 = f2_pack(sl2, sl2);
     uint32_t sph = 0, ofph = 0, qeph = 0;
     SegmentWalker walk(p);
     Segment S;
@@ -360,18 +359,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const float base = (m_used == -INFINITY) ? 0.f : m_used;
+        // Keys past Nkv are -inf and ex2(-inf) = 0, so the exp2 loop needs no
+        // mask; only scale 0 (0 * -inf) needs the visible logits set to 0
+        // with a unit factor.
+        float csl = sl2;
+        if (ragged && sl2 == 0.f) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i) v[i] = (v[i] == -INFINITY) ? -INFINITY : 0.f;
+          csl = 1.f;
+        }
+        const uint64_t c2 = f2_pack(csl, csl);
         const uint64_t nb2 = f2_pack(-base, -base);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[BN / 2];
 #pragma unroll
         for (int i = 0; i < BN / 2; ++i) {
           const uint64_t x = f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), c2, nb2);
-          float p0 = ex2(f2_lo(x));
-          float p1 = ex2(f2_hi(x));
-          if (ragged) {
-            if (key0 + 2 * i >= p.Nkv) p0 = 0.f;
-            if (key0 + 2 * i + 1 >= p.Nkv) p1 = 0.f;
-          }
+          const float p0 = ex2(f2_lo(x));
+          const float p1 = ex2(f2_hi(x));
           acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }

@@ -72,7 +72,10 @@ typedef enum {
  * Supported (d_qk, d_v): (64, 64) and (128, 128) through the prefill kernel,
  * any Nq and Nkv >= 1; (576, 512) with Nq == 1, non-causal, through the
  * split-KV decode kernel plus a combine kernel.  The decode path takes a
- * stream-ordered workspace (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * stream-ordered workspace (cudaMallocFromPoolAsync / cudaFreeAsync on
+ * `stream`) from a memory pool the library creates per device; the pool
+ * keeps freed memory for the next call (it never shrinks below the largest
+ * workspace used so far), so repeated calls map no new memory.
  *
  * Pointers must be 16-byte aligned (the tensor-memory-accelerator rule).
  * Returns ATTN_OK once the kernels are enqueued.  Device-side failures are
@@ -118,7 +121,8 @@ size_t attn_decode_workspace_bytes(int B, int Hkv, int Nkv);
  * call time - a host framework whose caching allocator already holds the
  * GPU's free memory, a serving loop with a fixed memory budget that must not
  * fail in the middle of a request, or a plug-in whose host forbids
- * allocation.  attn_fwd takes its decode workspace from cudaMallocAsync;
+ * allocation.  attn_fwd takes its decode workspace from a stream-ordered
+ * pool (cudaMallocFromPoolAsync);
  * this entry point calls no cudaMalloc, cudaFree or any allocating routine.
  *
  * Its split partials go to one static device array of 48 MiB declared in

@@ -5,7 +5,7 @@ framework whose caching allocator already holds the GPU's free memory, a
 serving loop with a fixed memory budget, a plug-in whose host forbids
 allocation).  For them the library's split-KV decode has a variant whose
 partial results live in a fixed static device array instead of a
-cudaMallocAsync workspace.  These checks call it through the C ABI and hold
+stream-ordered pool workspace.  These checks call it through the C ABI and hold
 its output to the same tolerance as every other parity test, against the
 regular attn_fwd path, on two calls in a row (the array keeps the previous
 call's contents, so the second call must not depend on it being clear).
