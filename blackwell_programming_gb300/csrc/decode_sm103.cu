@@ -239,8 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     Segment S;
     bool ok = true;
     while (ok && walk.next(S)) {
-      if (!(ok = warp_wait(bar(B_OEMPTY), oeph ^ 1u, wctx))) break;
-      oeph ^= 1u;
       if (!(ok = warp_wait(bar(B_QFULL), qph, wctx))) break;
       qph ^= 1u;
       if (!(ok = warp_wait(bar(B_QTFULL), qtph, wctx))) break;
@@ -272,6 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O += P V: P (64 keys, bf16 pairs) from TMEM over S, V = ring B
         if (!(ok = warp_wait(bar(B_PFULL), pph, wctx))) break;
         pph ^= 1u;
+        if (j == 0) {
+          // the previous segment's epilogue must have read O
+          if (!(ok = warp_wait(bar(B_OEMPTY), oeph ^ 1u, wctx))) break;
+          oeph ^= 1u;
+        }
         tc_fence_after();
         const uint64_t vd = v_desc0 + ((bs * B_BYTES) >> 4);
 #pragma unroll
@@ -293,32 +296,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = (warp * 32u) << 16;
     const float sl2 = p.scale_log2;
     uint32_t sph = 0, ofph = 0, qeph = 0;
-    SegmentWalker walk(p);
-    Segment S;
-    bool ok = true;
-    while (ok && walk.next(S)) {
-      // Q features 0..383 of this head into TMEM (bf16 pairs, column c = features
-      // 2c, 2c+1) once the previous segment's last Q K^T has finished.
-      if (!(ok = warp_wait(bar(B_QEMPTY), qeph ^ 1u, wctx))) break;
+    // Q features 0..383 of row r into TMEM (bf16 pairs, column COL_Q + c
+    // holds features 2c, 2c+1), once the previous segment's last Q K^T has
+    // finished: two rounds of 24 loads of 16 bytes in flight.
+    auto load_q = [&](const Segment& s) -> bool {
+      if (!warp_wait(bar(B_QEMPTY), qeph ^ 1u, wctx)) return false;
       qeph ^= 1u;
       tc_fence_after();
-      {
-        const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(S.plane) * p.group + (live ? r : 0)) * DQK);
+      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(s.plane) * p.group + (live ? r : 0)) * DQK);
 #pragma unroll 1
-        for (int c = 0; c < Q_TMEM_FEATS / 64; ++c) {
-          uint32_t w[32];
+      for (int b = 0; b < 2; ++b) {
+        uint32_t w[3][32];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint4 x = live ? qrow[c * 8 + i] : make_uint4(0u, 0u, 0u, 0u);
-            w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
-          }
-          tmem_st32u(tm + lane_addr + COL_Q + c * 32, w);
+        for (int i = 0; i < 24; ++i) {
+          const uint4 x = live ? qrow[b * 24 + i] : make_uint4(0u, 0u, 0u, 0u);
+          w[i >> 3][4 * (i & 7)] = x.x;
+          w[i >> 3][4 * (i & 7) + 1] = x.y;
+          w[i >> 3][4 * (i & 7) + 2] = x.z;
+          w[i >> 3][4 * (i & 7) + 3] = x.w;
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_QTFULL));
+#pragma unroll
+        for (int t = 0; t < 3; ++t) tmem_st32u(tm + lane_addr + COL_Q + (b * 3 + t) * 32, w[t]);
       }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QTFULL));
+      return true;
+    };
+    SegmentWalker walk(p);
+    Segment S, Snext;
+    bool have = walk.next(S);
+    bool ok = true;
+    if (have) ok = load_q(S);
+    while (ok && have) {
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < S.n; ++j) {
         if (!(ok = warp_wait(bar(B_SFULL), sph, wctx))) break;
@@ -389,27 +400,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(B_PFULL));
       }
       if (!ok) break;
+      // The next segment's Q first, so that its first Q K^T overlaps this
+      // segment's epilogue.
+      have = walk.next(Snext);
+      if (have && !(ok = load_q(Snext))) break;
       if (!(ok = warp_wait(bar(B_OFULL), ofph, wctx))) break;
       ofph ^= 1u;
       tc_fence_after();
+      // Partial O, normalised, in a layout where the float4 of row r and
+      // columns 4c..4c+3 sits at [slot][c][r]: a warp's 32 rows store 512
+      // contiguous bytes at a time.
       const size_t slot = static_cast<size_t>(blockIdx.x) * p.max_seg + S.slot;
-      float* orow = p.o_part + (slot * BM + r) * DVH;
+      float4* opart = reinterpret_cast<float4*>(p.o_part) + slot * (DVH / 4) * BM + r;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll 1
       for (int c = 0; c < DVH / 32; ++c) {
         float o[32];
         tmem_ld32(tm + lane_addr + COL_O + c * 32, o);
         if (live) {
-          float4* dst = reinterpret_cast<float4*>(orow + c * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(o[4 * i] * inv_l, o[4 * i + 1] * inv_l, o[4 * i + 2] * inv_l, o[4 * i + 3] * inv_l);
+            opart[static_cast<size_t>(c * 8 + i) * BM] =
+                make_float4(o[4 * i] * inv_l, o[4 * i + 1] * inv_l, o[4 * i + 2] * inv_l, o[4 * i + 3] * inv_l);
         }
       }
       if (live) p.lse_part[slot * BM + r] = (l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_OEMPTY));
+      S = Snext;
     }
   }
 
@@ -421,77 +440,91 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// One warp per output row and value half: lanes read the row's partial LSEs
-// (32 at a time), reduce the maximum and the sum of weights with shuffles,
-// and each lane merges its 8 of the 256 columns with float4 loads.  `grid` is the decode kernel's grid
-// size, which fixes where the partials are.
-constexpr int kCombineWarps = 8;
+// Combine: one warp per (value half, plane, 32 output rows, 32 output
+// columns), one lane per row.  A lane reduces its row's partial LSEs (a few
+// per row) and merges its row's 32 columns: float4 reads of the partials
+// that are coalesced across the lanes (their rows are adjacent in the partial
+// layout), a transpose through shared memory, and one 128-byte store per
+// row.  `grid` is the decode kernel's grid size, which fixes where the
+// partials are.
+constexpr int kCombineWarps = 4;
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecodeParams p, int grid, float* o,
                                                                      float* lse) {
-  const int wid = blockIdx.x * kCombineWarps + static_cast<int>(threadIdx.x >> 5);
+  __shared__ float tile[kCombineWarps][32][33];
+  const int wib = static_cast<int>(threadIdx.x >> 5);
+  const int wid = blockIdx.x * kCombineWarps + wib;
   const int lane = static_cast<int>(threadIdx.x & 31);
-  const int rows = p.planes * p.group;
-  if (wid >= 2 * rows) return;
-  const int half = wid / rows;
-  const int rr = wid - half * rows;
-  const int plane = rr / p.group;
-  const int r = rr - plane * p.group;
+  const int rblocks = (p.group + 31) / 32;
+  constexpr int kColBlocks = DVH / 32;
+  if (wid >= 2 * p.planes * rblocks * kColBlocks) return;
+  const int blk = wid % kColBlocks;
+  const int rb = wid / kColBlocks;
+  const int half = rb / (p.planes * rblocks);
+  const int rest = rb - half * p.planes * rblocks;
+  const int plane = rest / rblocks;
+  const int r0 = (rest - plane * rblocks) * 32;
+  const int r = r0 + lane;
+  const bool live = r < p.group;
+  const int rr = live ? r : r0;   // dead lanes read a live row and write nothing
   const long long tiles = p.tiles;
   const long long total = 2LL * p.planes * tiles;
   const long long sg = static_cast<long long>(half) * p.planes + plane;
   const long long gs = sg * tiles, ge = gs + tiles - 1;
   const int c_first = static_cast<int>(((gs + 1) * grid + total - 1) / total - 1);
   const int c_last = static_cast<int>(((ge + 1) * grid + total - 1) / total - 1);
-  const int count = c_last - c_first + 1;   // CTAs whose range meets this segment
-  // Partial i (0 <= i < count) belongs to CTA c_first + i; lanes take them
-  // 32 at a time.
-  auto partial = [&](int i, size_t& slot) -> float {
+  // Partial slot of the i-th CTA whose range meets this (half, plane), or -1.
+  auto slot_of = [&](int i) -> long long {
     const int cta = c_first + i;
     const long long b0 = range_begin(total, cta, grid), b1 = range_begin(total, cta + 1, grid);
-    if (b1 <= b0) return -INFINITY;
-    slot = static_cast<size_t>(cta) * p.max_seg + static_cast<size_t>(sg - b0 / tiles);
-    return p.lse_part[slot * BM + r];
+    if (b1 <= b0) return -1;
+    return static_cast<long long>(cta) * p.max_seg + (sg - b0 / tiles);
   };
   float mx = -INFINITY;
-  for (int base = 0; base < count; base += 32) {
-    size_t slot = 0;
-    if (base + lane < count) mx = fmaxf(mx, partial(base + lane, slot));
+  for (int i = 0; i <= c_last - c_first; ++i) {
+    const long long s = slot_of(i);
+    if (s >= 0) mx = fmaxf(mx, p.lse_part[s * BM + rr]);
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
   float tot = 0.f;
-  float4 acc0 = make_float4(0.f, 0.f, 0.f, 0.f), acc1 = acc0;
   if (mx != -INFINITY) {
-    for (int base = 0; base < count; base += 32) {
-      size_t my_slot = 0;
-      float w = 0.f;
-      if (base + lane < count) {
-        const float l = partial(base + lane, my_slot);
-        w = (l == -INFINITY) ? 0.f : expf(l - mx);
-      }
-      tot += w;
-      const int m = min(32, count - base);
-      for (int i = 0; i < m; ++i) {
-        const float wi = __shfl_sync(kFull, w, i);
-        const unsigned long long si = __shfl_sync(kFull, static_cast<unsigned long long>(my_slot), i);
-        if (wi == 0.f) continue;
-        const float4* src =
-            reinterpret_cast<const float4*>(p.o_part + (static_cast<size_t>(si) * BM + r) * DVH) + lane * 2;
-        const float4 x = src[0], y = src[1];
-        acc0.x += wi * x.x; acc0.y += wi * x.y; acc0.z += wi * x.z; acc0.w += wi * x.w;
-        acc1.x += wi * y.x; acc1.y += wi * y.y; acc1.z += wi * y.z; acc1.w += wi * y.w;
+    for (int i = 0; i <= c_last - c_first; ++i) {
+      const long long s = slot_of(i);
+      if (s < 0) continue;
+      const float ls = p.lse_part[s * BM + rr];
+      if (ls != -INFINITY) tot += expf(ls - mx);
+    }
+  }
+  const float inv = (tot > 0.f) ? 1.f / tot : 0.f;
+  float* out_rows = o + (static_cast<size_t>(plane) * p.group + r0) * (2 * DVH) + half * DVH;
+  float4 acc[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (mx != -INFINITY) {
+    for (int i = 0; i <= c_last - c_first; ++i) {
+      const long long s = slot_of(i);
+      if (s < 0) continue;
+      const float ls = p.lse_part[s * BM + rr];
+      if (ls == -INFINITY) continue;
+      const float w = expf(ls - mx) * inv;
+      const float4* src = reinterpret_cast<const float4*>(p.o_part) + (s * (DVH / 4) + blk * 8) * BM + rr;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float4 x = src[static_cast<size_t>(c) * BM];
+        acc[c].x += w * x.x; acc[c].y += w * x.y; acc[c].z += w * x.z; acc[c].w += w * x.w;
       }
     }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(kFull, tot, off);
-  const float inv = (tot > 0.f) ? 1.f / tot : 0.f;
-  acc0.x *= inv; acc0.y *= inv; acc0.z *= inv; acc0.w *= inv;
-  acc1.x *= inv; acc1.y *= inv; acc1.z *= inv; acc1.w *= inv;
-  float4* dst = reinterpret_cast<float4*>(o + static_cast<size_t>(rr) * (2 * DVH) + half * DVH) + lane * 2;
-  dst[0] = acc0;
-  dst[1] = acc1;
-  if (half == 0 && lane == 0 && lse != nullptr) lse[rr] = (tot > 0.f) ? mx + logf(tot) : -INFINITY;
+  for (int c = 0; c < 8; ++c) {
+    tile[wib][lane][4 * c] = acc[c].x;
+    tile[wib][lane][4 * c + 1] = acc[c].y;
+    tile[wib][lane][4 * c + 2] = acc[c].z;
+    tile[wib][lane][4 * c + 3] = acc[c].w;
+  }
+  __syncwarp();
+  for (int row = 0; row < 32 && r0 + row < p.group; ++row)
+    out_rows[static_cast<size_t>(row) * (2 * DVH) + blk * 32 + lane] = tile[wib][row][lane];
+  if (half == 0 && blk == 0 && live && lse != nullptr)
+    lse[static_cast<size_t>(plane) * p.group + r] = (tot > 0.f) ? mx + logf(tot) : -INFINITY;
 }
 
 }  // namespace
@@ -521,7 +554,7 @@ cudaError_t launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const De
 }
 
 cudaError_t launch_combine(const DecodeParams& p, int grid, float* o, float* lse, cudaStream_t stream) {
-  const int warps = 2 * p.planes * p.group;
+  const int warps = 2 * p.planes * ((p.group + 31) / 32) * (DVH / 32);
   combine_kernel<<<(warps + kCombineWarps - 1) / kCombineWarps, kCombineWarps * 32, 0, stream>>>(p, grid, o, lse);
   return cudaGetLastError();
 }
