@@ -21,8 +21,11 @@
 //  * Warps 8 and 10 issue the tcgen05.mma of query tile 0 and 1 (warp-uniform
 //    code, one elected lane per instruction).  S_t = Q_t K_j^T lands in
 //    tensor memory (TMEM); the softmax writes P_t (bf16) over S_t and the
-//    MMA computes O_t += P_t V_j with P read straight from TMEM.  The two query tiles ping-pong: the tensor core
-//    works on one tile while the softmax warpgroup of the other one runs.
+//    MMA computes O_t += P_t V_j with P read straight from TMEM.  The two
+//    query tiles ping-pong: the tensor core works on one tile while the
+//    softmax warpgroup of the other one runs.  P_t is published in two
+//    halves (keys 0..63, then 64..127), and P V starts on the first half
+//    while the softmax computes the second.
 //  * Warpgroups 0 and 1 own query tile 0 and 1.  TMEM lane i is row i, so a
 //    thread owns a whole row: max, exp2 and sum stay in-thread.  They also
 //    rescale O (only when the running max grew by more than 2^8, which keeps
@@ -69,7 +72,7 @@ struct Cfg {
   static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 4 + KS, B_VFULL = 4 + 2 * KS,
                        B_VEMPTY = 4 + 2 * KS + VS, B_SFULL = 4 + 2 * KS + 2 * VS, B_PFULL = B_SFULL + 2,
                        B_OFULL = B_PFULL + 2, B_OEMPTY = B_OFULL + 2, B_DRAIN = B_OEMPTY + 2,
-                       B_TURN = B_DRAIN + 1, NUM_BARS = B_TURN + 2;
+                       B_TURN = B_DRAIN + 1, B_PHALF = B_TURN + 2, NUM_BARS = B_PHALF + 2;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alignment
   // TMEM column of S_t and O_t
@@ -143,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::B_QEMPTY + t), 1);
       mbar_init(bar(C::B_SFULL + t), 1);
       mbar_init(bar(C::B_PFULL + t), 4);
+      mbar_init(bar(C::B_PHALF + t), 4);
       mbar_init(bar(C::B_OFULL + t), 1);
       mbar_init(bar(C::B_OEMPTY + t), 4);
     }
@@ -278,8 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               oeph ^= 1u;
               o_waited = true;
             }
-            if (!(ok = warp_wait(bar(C::B_PFULL + t), pph, wctx))) break;
-            pph ^= 1u;
+            if (!(ok = warp_wait(bar(C::B_PHALF + t), pph, wctx))) break;
           }
           if (do_s && j == 0) {
             if (!(ok = warp_wait(bar(C::B_QFULL + t), qph, wctx))) break;
@@ -290,10 +293,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (do_pv) {
             // O_t += P_t(j-1) V_{j-1}; P read from TMEM over S_t
+            // keys 0..63 as soon as their P is in TMEM, keys 64..127 after
             const uint64_t vd = v_desc0 + ((vs * C::KV_BYTES) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
+            for (int kk = 0; kk < BN / 32; ++kk)
               mma_ts_warp(dO, dS + kk * 8, vd + ((kk * 16 * 128) >> 4), C::IDESC_PV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+            if (!(ok = warp_wait(bar(C::B_PFULL + t), pph, wctx))) break;
+            pph ^= 1u;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = BN / 32; kk < BN / 16; ++kk)
+              mma_ts_warp(dO, dS + kk * 8, vd + ((kk * 16 * 128) >> 4), C::IDESC_PV, 1u);
           }
           if (do_s) {
             // S_t = Q_t K_j^T
@@ -414,22 +424,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t c2 = f2_pack(csl, csl);
         const uint64_t nb2 = f2_pack(-base, -base);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pk[BN / 2];
+        // P in two halves: keys 0..63 are published first, so the MMA warp
+        // can start P V on them while keys 64..127 are computed.
 #pragma unroll
-        for (int i = 0; i < BN / 2; ++i) {
-          const uint64_t x = f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), c2, nb2);
-          const float p0 = ex2(f2_lo(x));
-          const float p1 = ex2(f2_hi(x));
-          acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[BN / 4];
+#pragma unroll
+          for (int i = 0; i < BN / 4; ++i) {
+            const int e = h * (BN / 4) + i;
+            const uint64_t x = f2_fma(f2_pack(v[2 * e], v[2 * e + 1]), c2, nb2);
+            const float p0 = ex2(f2_lo(x));
+            const float p1 = ex2(f2_hi(x));
+            acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32u(tS + h * (BN / 4), pk);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(h == 0 ? C::B_PHALF + t : C::B_PFULL + t));
         }
-        tmem_st64(tS, pk);
         const uint64_t a01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
         l += f2_lo(a01) + f2_hi(a01);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_PFULL + t));
       }
       if (!ok) break;
       // epilogue: O / l and LSE, then hand O_t back to the MMA warp
