@@ -453,22 +453,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       ofph ^= 1u;
       tc_fence_after();
       const bool live = row < p.Nq;
-      float* orow = p.o + (static_cast<size_t>(U.b * p.Hq + U.h) * p.Nq + (live ? row : 0)) * D;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      // O leaves TMEM in the 16x256b shape: each store instruction of the
+      // warp then writes 8 rows x 32 contiguous bytes (whole sectors),
+      // instead of 32 rows x 16 bytes with one row per thread.
+      float* ohead = p.o + static_cast<size_t>(U.b * p.Hq + U.h) * p.Nq * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float v[32];
-        if (n > 0) {
-          tmem_ld32(tO + c * 32, v);
-        } else {
+      for (int hl = 0; hl < 2; ++hl) {
+        const int ra = static_cast<int>(quad * 32 + hl * 16 + (lane >> 2));   // rows ra and ra + 8 of the tile
+        const float ia = __shfl_sync(kFull, inv_l, hl * 16 + (lane >> 2));
+        const float ib = __shfl_sync(kFull, inv_l, hl * 16 + (lane >> 2) + 8);
+        const bool la = q0 + ra < p.Nq, lb = q0 + ra + 8 < p.Nq;
+        float* oa = ohead + static_cast<size_t>(la ? q0 + ra : 0) * D + 2 * (lane & 3);
+        float* ob = ohead + static_cast<size_t>(lb ? q0 + ra + 8 : 0) * D + 2 * (lane & 3);
+#pragma unroll 1
+        for (int ch = 0; ch < D / 64; ++ch) {
+          uint32_t r[32];
+          if (n > 0) {
+            tmem_ld16x256b_x8(tm + ((quad * 32u + hl * 16u) << 16) + C::col_o(t) + ch * 64, r);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
-        }
-        if (live) {
-          float4* dst = reinterpret_cast<float4*>(orow + c * 32);
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(v[4 * i] * inv_l, v[4 * i + 1] * inv_l, v[4 * i + 2] * inv_l, v[4 * i + 3] * inv_l);
+          for (int k = 0; k < 8; ++k) {
+            if (la)
+              *reinterpret_cast<float2*>(oa + ch * 64 + 8 * k) =
+                  make_float2(__uint_as_float(r[4 * k]) * ia, __uint_as_float(r[4 * k + 1]) * ia);
+            if (lb)
+              *reinterpret_cast<float2*>(ob + ch * 64 + 8 * k) =
+                  make_float2(__uint_as_float(r[4 * k + 2]) * ib, __uint_as_float(r[4 * k + 3]) * ib);
+          }
         }
       }
       if (live && p.lse != nullptr) {
