@@ -282,37 +282,52 @@ __global__ void __launch_bounds__(kThreads, 1)
               oeph ^= 1u;
               o_waited = true;
             }
-            if (!(ok = warp_wait(bar(C::B_PHALF + t), pph, wctx))) break;
           }
           if (do_s && j == 0) {
             if (!(ok = warp_wait(bar(C::B_QFULL + t), qph, wctx))) break;
             qph ^= 1u;
           }
+          // The turn before P: it is normally free long before P is ready,
+          // and taking it first leaves only the P wait between the softmax
+          // and the first P V.
           if (!(ok = warp_wait(bar(C::B_TURN + t), tph, wctx))) break;
           tph ^= 1u;
+          if (do_pv && !(ok = warp_wait(bar(C::B_PHALF + t), pph, wctx))) break;
           tc_fence_after();
           if (do_pv) {
             // O_t += P_t(j-1) V_{j-1}; P read from TMEM over S_t
             // keys 0..63 as soon as their P is in TMEM, keys 64..127 after
             const uint64_t vd = v_desc0 + ((vs * C::KV_BYTES) >> 4);
+            {
+              uint32_t a[4];
+              uint64_t b[4];
 #pragma unroll
-            for (int kk = 0; kk < BN / 32; ++kk)
-              mma_ts_warp(dO, dS + kk * 8, vd + ((kk * 16 * 128) >> 4), C::IDESC_PV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < 4; ++kk) { a[kk] = dS + kk * 8; b[kk] = vd + ((kk * 16 * 128) >> 4); }
+              mma_ts_warp4(dO, a, b, C::IDESC_PV, j - 1 > 0 ? 1u : 0u);
+            }
             if (!(ok = warp_wait(bar(C::B_PFULL + t), pph, wctx))) break;
             pph ^= 1u;
             tc_fence_after();
+            {
+              uint32_t a[4];
+              uint64_t b[4];
 #pragma unroll
-            for (int kk = BN / 32; kk < BN / 16; ++kk)
-              mma_ts_warp(dO, dS + kk * 8, vd + ((kk * 16 * 128) >> 4), C::IDESC_PV, 1u);
+              for (int kk = 0; kk < 4; ++kk) { a[kk] = dS + (4 + kk) * 8; b[kk] = vd + (((4 + kk) * 16 * 128) >> 4); }
+              mma_ts_warp4(dO, a, b, C::IDESC_PV, 1u);
+            }
           }
           if (do_s) {
-            // S_t = Q_t K_j^T
+            // S_t = Q_t K_j^T, one 64-feature chunk (four MMAs) per elect
             const uint64_t kd = k_desc0 + ((ks * C::KV_BYTES) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off_q = ((kk >> 2) * C::CHUNK_Q + (kk & 3) * 32) >> 4;
-              const uint32_t off_k = ((kk >> 2) * C::CHUNK_KV + (kk & 3) * 32) >> 4;
-              mma_ss_warp(dS, q_desc + off_q, kd + off_k, C::IDESC_S, kk > 0 ? 1u : 0u);
+            for (int kc = 0; kc < C::KCH; ++kc) {
+              uint64_t a[4], b[4];
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                a[kk] = q_desc + ((kc * C::CHUNK_Q + kk * 32) >> 4);
+                b[kk] = kd + ((kc * C::CHUNK_KV + kk * 32) >> 4);
+              }
+              mma_ss_warp4(dS, a, b, C::IDESC_S, kc > 0 ? 1u : 0u);
             }
           }
           mbar_arrive_warp(bar(C::B_TURN + (t ^ 1)));

@@ -229,6 +229,32 @@ __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Four MMAs behind one elect.sync (warp-uniform call).  The first takes the
+// accumulate flag `acc0`, the other three accumulate.
+__device__ __forceinline__ void mma_ss_warp4(uint32_t d_tmem, const uint64_t (&a)[4], const uint64_t (&b)[4],
+                                             uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, q;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.ne.b32 q, %11, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, q;\n\t}" ::"r"(d_tmem),
+      "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(acc0),
+      "r"(1u)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_warp4(uint32_t d_tmem, const uint32_t (&a)[4], const uint64_t (&b)[4],
+                                             uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, q;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.ne.b32 q, %11, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %9, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %9, q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %9, q;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %9, q;\n\t}" ::"r"(d_tmem),
+      "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(acc0),
+      "r"(1u)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
