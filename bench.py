@@ -38,7 +38,8 @@ L2_FLUSH_BYTES = 256 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {"prefill": "blackwell_programming_gb300/csrc/prefill_sm103.cu",
-                  "decode": "blackwell_programming_gb300/csrc/decode_sm103.cu"}
+                  "decode": "blackwell_programming_gb300/csrc/decode_sm103.cu",
+                  "latent_prefill": "blackwell_programming_gb300/csrc/decode_sm103.cu"}
 
 
 # ----------------------------------------------------------------- helpers
@@ -340,14 +341,14 @@ def run_ours(args, wl):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     peaks, peak_src = load_peaks()
-    kind = "decode" if wl.d_qk == 576 else "prefill"
+    kind = ("decode" if wl.Nq == 1 else "latent_prefill") if wl.d_qk == 576 else "prefill"
     per_launch = total / args.steps
-    if kind == "prefill":
+    if kind in ("prefill", "latent_prefill"):
         achieved = flops / per_launch / 1e12
+        kname = {64: "prefill_kernel<64>", 128: "prefill_kernel<128>"}.get(wl.d_qk, "latent_kernel (prefill mode)")
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "peak_source": peak_src + " bf16_tflops (burst)",
-                "kernel": "prefill_kernel<128>" if wl.d_qk == 128 else "prefill_kernel<64>",
-                "algorithmic_flops_per_launch": flops}
+                "kernel": kname, "algorithmic_flops_per_launch": flops}
     else:
         achieved = wl.algorithmic_bytes / per_launch / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -356,7 +357,7 @@ def run_ours(args, wl):
                 "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
                 "tensor_tflops": flops / per_launch / 1e12}
     roof["traffic"] = committed_traffic(kind, wl.name)
-    launches = (1 if kind == "prefill" else 2) * args.steps
+    launches = (2 if kind == "decode" else 1) * args.steps
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

@@ -207,13 +207,12 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, 
     return ATTN_ERR_UNSUPPORTED;
 
   const bool prefill = (d_qk == d_v) && (d_qk == 64 || d_qk == 128);
-  const bool decode = (d_qk == 576 && d_v == 512);
-  if (!prefill && !decode) return ATTN_ERR_UNSUPPORTED;
-  if (decode) {
-    // One query per sequence: with the bottom-right causal alignment it sees
-    // every key, so the causal flag changes nothing.
-    if (Nq != 1 || !v_aliases_k || Hq / Hkv > 128) return ATTN_ERR_UNSUPPORTED;
-  }
+  const bool latent = (d_qk == 576 && d_v == 512);
+  if (!prefill && !latent) return ATTN_ERR_UNSUPPORTED;
+  if (latent && !v_aliases_k) return ATTN_ERR_UNSUPPORTED;
+  // One query per sequence sees every key under the bottom-right causal
+  // alignment, so the causal flag changes nothing for the split-KV decode.
+  const bool decode = latent && Nq == 1 && Hq / Hkv <= 128;
 
   DeviceInfo* dev = nullptr;
   int st = device_info(&dev);
@@ -246,6 +245,30 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, 
     p.err = dev->err;
     if ((e = launch_prefill(d, tq, tk, tv, p, dev->num_sms, stream)) != cudaSuccess)
       return cuda_fail(e, "prefill launch");
+  } else if (!decode) {
+    // latent shape, Nq > 1: the decode kernel in prefill mode
+    CUtensorMap tq, tk;
+    const uint64_t rs = static_cast<uint64_t>(d_qk) * 2;
+    if ((st = make_map(&tq, q, d_qk, Nq, static_cast<uint64_t>(B) * Hq, rs, rs * Nq, 128)) != ATTN_OK) return st;
+    if ((st = make_map(&tk, k, d_qk, Nkv, static_cast<uint64_t>(B) * Hkv, rs, rs * Nkv, decode_key_tile())) != ATTN_OK)
+      return st;
+    LatentPrefillParams p{};
+    p.q = static_cast<const uint16_t*>(q);
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Nq = Nq;
+    p.Nkv = Nkv;
+    p.causal = causal ? 1 : 0;
+    p.tiles = decode_tiles(Nkv);
+    p.nqb = (Nq + 127) / 128;
+    p.num_units = 2 * B * Hq * p.nqb;
+    p.scale_log2 = scale_log2;
+    p.err = dev->err;
+    if ((e = launch_latent_prefill(tq, tk, p, dev->num_sms, stream)) != cudaSuccess)
+      return cuda_fail(e, "latent prefill launch");
   } else {
     const int group = Hq / Hkv;
     const int planes = B * Hkv;

@@ -1,6 +1,7 @@
-// decode_sm103.cu - split-KV attention decode for the latent head-dim shape
-// (d_qk = 576, d_v = 512, V = the first 512 features of K), and the combine
-// kernel that merges the splits.
+// decode_sm103.cu - attention for the latent head-dim shape (d_qk = 576,
+// d_v = 512, V = the first 512 features of K): the split-KV decode with the
+// combine kernel that merges its splits, and the prefill (causal or not,
+// Nq > 1) that runs the same kernel on blocks of 128 query rows.
 //
 // The shape is the DeepSeek MLA case of "Distilling a 4.5 hour CUDA talk",
 // sections 12-13: Q/K are 576 wide and V/O are the first 512 features.  That
@@ -22,11 +23,19 @@
 // kernel then merges the partials of each row:
 //   LSE = log sum_s exp(lse_s),   O = sum_s exp(lse_s - LSE) O_s.
 //
+// Prefill mode: a work item is (value half, batch, query head, block of 128
+// query rows) and covers every K tile the block sees (all of them, or up to
+// the causal diagonal with bottom-right alignment), so it writes O and LSE
+// directly.  Items are handed out longest first (query blocks from the
+// bottom), the two halves of a block and the heads that share a KV head
+// side by side so that their K tiles come from L2.
+//
 // Roles: warp 5 = TMA producer (the shared-memory part of Q once per
 // segment, K tiles through two rings), warp 4 = tcgen05 MMA issuer (whole
 // warp, one elected lane per instruction), warps 0-3 = the TMEM part of Q,
 // softmax (one row per thread), O rescale and epilogue.
 #include <cmath>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -90,7 +99,10 @@ __host__ __device__ __forceinline__ long long range_begin(long long total, int c
 struct Segment {
   int plane, half;
   int t0, n;    // first tile, tile count
-  int slot;     // partial slot within this CTA
+  int slot;     // partial slot within this CTA (decode)
+  int kplane;   // K plane (batch * Hkv + KV head)
+  int qplane;   // plane of the Q map: decode = KV plane (rows = heads), prefill = batch * Hq + head
+  int qrow0;    // first query row of the tile in that plane
 };
 
 struct SegmentWalker {
@@ -113,10 +125,63 @@ struct SegmentWalker {
     const long long end = min(g1, (sg + 1) * tiles);
     s.n = static_cast<int>(end - g);
     s.slot = static_cast<int>(sg - g0 / tiles);
+    s.kplane = s.qplane = s.plane;
+    s.qrow0 = 0;
     g = end;
     return true;
   }
 };
+
+// Prefill mode: unit u = ((query block from the bottom) * B * Hq + batch *
+// Hq + head) * 2 + half, handed to the persistent CTAs in rounds of
+// gridDim.x with every other round reversed (snake), so each CTA gets a
+// similar mix of long and short blocks.
+struct UnitWalker {
+  const LatentPrefillParams& p;
+  int it = 0;
+  __device__ UnitWalker(const LatentPrefillParams& prm) : p(prm) {}
+  __device__ bool next(Segment& s) {
+    const int base = it * static_cast<int>(gridDim.x);
+    const int u = (it & 1) ? base + static_cast<int>(gridDim.x - 1 - blockIdx.x) : base + static_cast<int>(blockIdx.x);
+    ++it;
+    if (u >= p.num_units) return false;
+    const int bh_count = p.B * p.Hq;
+    s.half = u & 1;
+    const int rest = u >> 1;
+    const int qb = p.nqb - 1 - rest / bh_count;
+    const int bh = rest - (rest / bh_count) * bh_count;
+    const int b = bh / p.Hq, h = bh - b * p.Hq;
+    s.qplane = bh;
+    s.kplane = b * p.Hkv + h / (p.Hq / p.Hkv);
+    s.plane = s.kplane;
+    s.qrow0 = qb * BM;
+    s.t0 = 0;
+    s.slot = 0;
+    int n = p.tiles;
+    if (p.causal) {
+      const int last_key = min(s.qrow0 + BM - 1, p.Nq - 1) + (p.Nkv - p.Nq);
+      n = last_key < 0 ? 0 : min(last_key / BN + 1, p.tiles);
+    }
+    s.n = n;
+    return true;
+  }
+};
+
+template <class P> struct WalkerFor;
+template <> struct WalkerFor<DecodeParams> { using type = SegmentWalker; };
+template <> struct WalkerFor<LatentPrefillParams> { using type = UnitWalker; };
+
+// Row r of a tile's Q: its global address, and whether it exists.
+__device__ __forceinline__ const uint16_t* q_row(const DecodeParams& p, const Segment& s, int r) {
+  return p.q + (static_cast<size_t>(s.qplane) * p.group + r) * DQK;
+}
+__device__ __forceinline__ bool q_live(const DecodeParams& p, const Segment&, int r) { return r < p.group; }
+__device__ __forceinline__ const uint16_t* q_row(const LatentPrefillParams& p, const Segment& s, int r) {
+  return p.q + (static_cast<size_t>(s.qplane) * p.Nq + s.qrow0 + r) * DQK;
+}
+__device__ __forceinline__ bool q_live(const LatentPrefillParams& p, const Segment& s, int r) {
+  return s.qrow0 + r < p.Nq;
+}
 
 // K chunk c (features 64c .. 64c+63) of a tile lives in ring B when it belongs
 // to the item's value half (chunks 4*half .. 4*half+3), else in ring A.
@@ -132,9 +197,11 @@ __device__ __forceinline__ int a_index(int c, int half) { return c < 4 * half ? 
 // are also its V half (ring B, freed after P V), so the shared memory left
 // beside Q's last third holds enough tiles in flight to cover the memory
 // latency.
+template <class P>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const DecodeParams p) {
+    latent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, const P p) {
+  constexpr bool kPrefill = std::is_same<P, LatentPrefillParams>::value;
+  using Walker = typename WalkerFor<P>::type;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -179,7 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      const uint64_t pol_k = l2_policy_evict_first();   // each K tile is read by the two halves, then dead
+      // decode: each K tile is read by the two halves, then dead; prefill: K
+      // is read again by every query head of its KV head and every block
+      const uint64_t pol_k = kPrefill ? l2_policy_evict_last() : l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
       int as = 0, bs = 0;
       uint32_t aph = 0, bph = 0, qph = 0;
@@ -189,16 +258,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         filled |= 1u << b;
         fill_par = (fill_par & ~(1u << b)) | (par << b);
       };
-      SegmentWalker walk(p);
+      Walker walk(p);
       Segment S;
       bool ok = true;
       while (ok && walk.next(S)) {
+        if (S.n == 0) continue;   // a prefill block that sees no key: the softmax warps write it
         if (!(ok = mbar_wait(bar(B_QEMPTY), qph ^ 1u, wctx))) break;
         qph ^= 1u;
         mbar_arrive_expect_tx(bar(B_QFULL), QS_BYTES);
         note_fill(0, qph ^ 1u);
         for (int c = 0; c < Q_SMEM_CH; ++c)
-          tma_load_3d(sQ + c * CHUNK_Q, &tmQ, bar(B_QFULL), Q_TMEM_FEATS + c * 64, 0, S.plane, pol_q);
+          tma_load_3d(sQ + c * CHUNK_Q, &tmQ, bar(B_QFULL), Q_TMEM_FEATS + c * 64, S.qrow0, S.qplane, pol_q);
         for (int j = 0; j < S.n; ++j) {
           const int y = (S.t0 + j) * BN;
           if (!(ok = mbar_wait(bar(B_AEMPTY + as), aph ^ 1u, wctx))) break;
@@ -207,13 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < QCH; ++c)
             if (!in_ring_b(c, S.half))
               tma_load_3d(sA + as * A_BYTES + a_index(c, S.half) * CHUNK_K, &tmK, bar(B_AFULL + as), c * 64, y,
-                          S.plane, pol_k);
+                          S.kplane, pol_k);
           if (++as == AS) { as = 0; aph ^= 1u; }
           if (!(ok = mbar_wait(bar(B_BEMPTY + bs), bph ^ 1u, wctx))) break;
           mbar_arrive_expect_tx(bar(B_BFULL + bs), B_BYTES);
           note_fill(1 + AS + bs, bph);
           for (int c = 0; c < B_CH; ++c)
-            tma_load_3d(sB + bs * B_BYTES + c * CHUNK_K, &tmK, bar(B_BFULL + bs), (4 * S.half + c) * 64, y, S.plane,
+            tma_load_3d(sB + bs * B_BYTES + c * CHUNK_K, &tmK, bar(B_BFULL + bs), (4 * S.half + c) * 64, y, S.kplane,
                         pol_k);
           if (++bs == BS) { bs = 0; bph ^= 1u; }
         }
@@ -235,10 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t b_desc0 = smem_desc_sw128(sB, 16, 1024);
     const uint64_t v_desc0 = smem_desc_sw128(sB, CHUNK_K, 1024);
     const uint32_t dS = tm + COL_S, dO = tm + COL_O, aQ = tm + COL_Q;
-    SegmentWalker walk(p);
+    Walker walk(p);
     Segment S;
     bool ok = true;
     while (ok && walk.next(S)) {
+      if (S.n == 0) continue;
       if (!(ok = warp_wait(bar(B_QFULL), qph, wctx))) break;
       qph ^= 1u;
       if (!(ok = warp_wait(bar(B_QTFULL), qtph, wctx))) break;
@@ -292,7 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 4) {
     // ----------------------------- Q into TMEM, softmax, rescale, epilogue
     const int r = static_cast<int>(warp * 32 + lane);
-    const bool live = r < p.group;
     const uint32_t lane_addr = (warp * 32u) << 16;
     const float sl2 = p.scale_log2;
     uint32_t sph = 0, ofph = 0, qeph = 0;
@@ -303,7 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(bar(B_QEMPTY), qeph ^ 1u, wctx)) return false;
       qeph ^= 1u;
       tc_fence_after();
-      const uint4* qrow = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(s.plane) * p.group + (live ? r : 0)) * DQK);
+      const bool live = q_live(p, s, r);
+      const uint4* qrow = reinterpret_cast<const uint4*>(q_row(p, s, live ? r : 0));
 #pragma unroll 1
       for (int b = 0; b < 2; ++b) {
         uint32_t w[3][32];
@@ -324,13 +395,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_QTFULL));
       return true;
     };
-    SegmentWalker walk(p);
+    Walker walk(p);
+    // The next work item with at least one K tile.  A prefill block that
+    // sees no key (causal, Nq > Nkv) gets O = 0 and LSE = -inf here.
+    auto advance = [&](Segment& s) -> bool {
+      while (walk.next(s)) {
+        if (s.n > 0) return true;
+        if constexpr (kPrefill) {
+          if (q_live(p, s, r)) {
+            float* orow = p.o + (static_cast<size_t>(s.qplane) * p.Nq + s.qrow0 + r) * (2 * DVH) + s.half * DVH;
+#pragma unroll 4
+            for (int c = 0; c < DVH / 4; ++c) reinterpret_cast<float4*>(orow)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s.half == 0 && p.lse != nullptr) p.lse[static_cast<size_t>(s.qplane) * p.Nq + s.qrow0 + r] = -INFINITY;
+          }
+        }
+      }
+      return false;
+    };
     Segment S, Snext;
-    bool have = walk.next(S);
+    bool have = advance(S);
     bool ok = true;
     if (have) ok = load_q(S);
     while (ok && have) {
       float m_used = -INFINITY, l = 0.f;
+      // Last key row r may see: all of them, or up to the causal diagonal
+      // (bottom-right alignment); the tile needs the mask when its last key
+      // is past the limit of its first row.
+      int key_lim = p.Nkv - 1, causal_lim0 = p.Nkv - 1;
+      if constexpr (kPrefill) {
+        if (p.causal) {
+          key_lim = min(S.qrow0 + r + (p.Nkv - p.Nq), p.Nkv - 1);
+          causal_lim0 = S.qrow0 + (p.Nkv - p.Nq);
+        }
+      }
       for (int j = 0; j < S.n; ++j) {
         if (!(ok = warp_wait(bar(B_SFULL), sph, wctx))) break;
         sph ^= 1u;
@@ -338,11 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[BN];
         tmem_ld64(tm + lane_addr + COL_S, v);
         const int key0 = (S.t0 + j) * BN;
-        const bool ragged = key0 + BN > p.Nkv;
+        const bool ragged = key0 + BN - 1 > causal_lim0;
         if (ragged) {
 #pragma unroll
           for (int i = 0; i < BN; ++i)
-            if (key0 + i >= p.Nkv) v[i] = -INFINITY;
+            if (key0 + i > key_lim) v[i] = -INFINITY;
         }
         float mx8[8];
 #pragma unroll
@@ -402,29 +499,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // The next segment's Q first, so that its first Q K^T overlaps this
       // segment's epilogue.
-      have = walk.next(Snext);
+      have = advance(Snext);
       if (have && !(ok = load_q(Snext))) break;
       if (!(ok = warp_wait(bar(B_OFULL), ofph, wctx))) break;
       ofph ^= 1u;
       tc_fence_after();
-      // Partial O, normalised, in a layout where the float4 of row r and
-      // columns 4c..4c+3 sits at [slot][c][r]: a warp's 32 rows store 512
-      // contiguous bytes at a time.
-      const size_t slot = static_cast<size_t>(blockIdx.x) * p.max_seg + S.slot;
-      float4* opart = reinterpret_cast<float4*>(p.o_part) + slot * (DVH / 4) * BM + r;
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const float lse_r = (l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if constexpr (kPrefill) {
+        // O half of rows qrow0 .. qrow0+127, straight to the output.  O
+        // leaves TMEM in the 16x256b shape, so each warp store writes 8 rows
+        // x 32 contiguous bytes.
+        float* ohead = p.o + (static_cast<size_t>(S.qplane) * p.Nq) * (2 * DVH) + S.half * DVH;
 #pragma unroll 1
-      for (int c = 0; c < DVH / 32; ++c) {
-        float o[32];
-        tmem_ld32(tm + lane_addr + COL_O + c * 32, o);
-        if (live) {
+        for (int hl = 0; hl < 2; ++hl) {
+          const int ra = static_cast<int>(warp * 32 + hl * 16 + (lane >> 2));   // rows ra and ra + 8 of the tile
+          const float ia = __shfl_sync(kFull, inv_l, hl * 16 + (lane >> 2));
+          const float ib = __shfl_sync(kFull, inv_l, hl * 16 + (lane >> 2) + 8);
+          const bool la = S.qrow0 + ra < p.Nq, lb = S.qrow0 + ra + 8 < p.Nq;
+          float* oa = ohead + static_cast<size_t>(la ? S.qrow0 + ra : 0) * (2 * DVH) + 2 * (lane & 3);
+          float* ob = ohead + static_cast<size_t>(lb ? S.qrow0 + ra + 8 : 0) * (2 * DVH) + 2 * (lane & 3);
+#pragma unroll 1
+          for (int ch = 0; ch < DVH / 64; ++ch) {
+            uint32_t rr[32];
+            tmem_ld16x256b_x8(tm + ((warp * 32u + hl * 16u) << 16) + COL_O + ch * 64, rr);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            opart[static_cast<size_t>(c * 8 + i) * BM] =
-                make_float4(o[4 * i] * inv_l, o[4 * i + 1] * inv_l, o[4 * i + 2] * inv_l, o[4 * i + 3] * inv_l);
+            for (int k = 0; k < 8; ++k) {
+              if (la)
+                *reinterpret_cast<float2*>(oa + ch * 64 + 8 * k) =
+                    make_float2(__uint_as_float(rr[4 * k]) * ia, __uint_as_float(rr[4 * k + 1]) * ia);
+              if (lb)
+                *reinterpret_cast<float2*>(ob + ch * 64 + 8 * k) =
+                    make_float2(__uint_as_float(rr[4 * k + 2]) * ib, __uint_as_float(rr[4 * k + 3]) * ib);
+            }
+          }
         }
+        if (S.half == 0 && p.lse != nullptr && q_live(p, S, r))
+          p.lse[static_cast<size_t>(S.qplane) * p.Nq + S.qrow0 + r] = lse_r;
+      } else {
+        // Partial O, normalised, in a layout where the float4 of row r and
+        // columns 4c..4c+3 sits at [slot][c][r]: a warp's 32 rows store 512
+        // contiguous bytes at a time.
+        const bool live = q_live(p, S, r);
+        const size_t slot = static_cast<size_t>(blockIdx.x) * p.max_seg + S.slot;
+        float4* opart = reinterpret_cast<float4*>(p.o_part) + slot * (DVH / 4) * BM + r;
+#pragma unroll 1
+        for (int c = 0; c < DVH / 32; ++c) {
+          float o[32];
+          tmem_ld32(tm + lane_addr + COL_O + c * 32, o);
+          if (live) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              opart[static_cast<size_t>(c * 8 + i) * BM] =
+                  make_float4(o[4 * i] * inv_l, o[4 * i + 1] * inv_l, o[4 * i + 2] * inv_l, o[4 * i + 3] * inv_l);
+          }
+        }
+        if (live) p.lse_part[slot * BM + r] = lse_r;
       }
-      if (live) p.lse_part[slot * BM + r] = (l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_OEMPTY));
@@ -546,10 +677,21 @@ int decode_max_segments(int planes, int tiles, int grid) {
 
 cudaError_t launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const DecodeParams& p, int grid,
                           cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(latent_kernel<DecodeParams>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  decode_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(tq, tk, p);
+  latent_kernel<DecodeParams><<<grid, kThreads, SMEM_BYTES, stream>>>(tq, tk, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_latent_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const LatentPrefillParams& p,
+                                  int num_sms, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(latent_kernel<LatentPrefillParams>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  const int grid = min(p.num_units, num_sms);
+  if (grid <= 0) return cudaSuccess;
+  latent_kernel<LatentPrefillParams><<<grid, kThreads, SMEM_BYTES, stream>>>(tq, tk, p);
   return cudaGetLastError();
 }
 

@@ -41,6 +41,25 @@ struct DecodeParams {
   unsigned* err;
 };
 
+// Prefill (Nq > 1, causal or not) for the same latent shape, run by the
+// decode kernel on blocks of 128 query rows of one (batch, query head); each
+// work item writes its half of O and (half 0) the LSE directly.
+struct LatentPrefillParams {
+  const uint16_t* q;   // bf16 Q [B * Hq, Nq, 576]
+  float* o;            // fp32 O [B * Hq, Nq, 512]
+  float* lse;          // fp32 LSE [B * Hq, Nq], may be null
+  int B, Hq, Hkv, Nq, Nkv;
+  int causal;
+  int tiles;           // ceil(Nkv / decode_key_tile())
+  int nqb;             // ceil(Nq / 128)
+  int num_units;       // 2 * B * Hq * nqb
+  float scale_log2;    // scale * log2(e)
+  unsigned* err;
+};
+
+cudaError_t launch_latent_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const LatentPrefillParams& p,
+                                  int num_sms, cudaStream_t stream);
+
 // Number of partial slots each CTA needs for a grid of `grid` CTAs.
 int decode_max_segments(int planes, int tiles, int grid);
 int decode_tiles(int Nkv);

@@ -150,6 +150,9 @@ WORKLOADS = {
                                  q_factor=1.0 / math.sqrt(2.0), kv_factor=1.0 / math.sqrt(2.0)),
     "decode_d576": Workload("decode_d576", 64, 128, 1, 1, 8192, 576, 512, False, 1.0 / math.sqrt(192.0),
                             v_aliases_k=True),
+    # latent (MLA) prefill: causal, Nq = Nkv, the decode's 576/512 heads with V = K[..., :512]
+    "mla_prefill_causal": Workload("mla_prefill_causal", 1, 64, 1, 4096, 4096, 576, 512, True,
+                                   1.0 / math.sqrt(192.0), v_aliases_k=True),
 }
 
 

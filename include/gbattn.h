@@ -42,7 +42,8 @@ typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, Hq % Hkv != 0,
                                   misaligned pointer, bad scale, bad aliasing   */
-    ATTN_ERR_UNSUPPORTED = 2,  /* head dims not built, or causal decode shape   */
+    ATTN_ERR_UNSUPPORTED = 2,  /* head dims not built, or a 576/512 shape whose
+                                  V is not the first 512 features of K          */
     ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed             */
     ATTN_ERR_TIMEOUT = 4,      /* a kernel gave up on a bounded wait            */
     ATTN_ERR_NO_DEVICE = 5,    /* no sm_103 device is current                   */
@@ -70,8 +71,13 @@ typedef enum {
  *  scale >= 0 and finite; the logits are scale * q_i . k_j.
  *
  * Supported (d_qk, d_v): (64, 64) and (128, 128) through the prefill kernel,
- * any Nq and Nkv >= 1; (576, 512) with Nq == 1, non-causal, through the
- * split-KV decode kernel plus a combine kernel.  The decode path takes a
+ * any Nq and Nkv >= 1.  (576, 512) with V aliased to the first 512 features
+ * of K (v == k): Nq == 1 and Hq / Hkv <= 128 through the split-KV decode
+ * kernel plus a combine kernel (one query sees every key under the
+ * bottom-right causal alignment, so the causal flag changes nothing there);
+ * any other Nq, causal or not, through the same kernel in prefill mode on
+ * blocks of 128 query rows, which writes O and LSE directly.  The decode
+ * path takes a
  * stream-ordered workspace (cudaMallocFromPoolAsync / cudaFreeAsync on
  * `stream`) from a memory pool the library creates per device; the pool
  * keeps freed memory for the next call (it never shrinks below the largest

@@ -84,9 +84,9 @@ def test_invalid_arguments_rejected_before_any_cuda_call(lib, bad):
 
 @pytest.mark.parametrize("bad", [
     dict(d_qk=96, d_v=96), dict(d_qk=128, d_v=64), dict(d_qk=256, d_v=256),
-    dict(d_qk=576, d_v=512, Nq=2),                        # latent shape: decode only
-    dict(d_qk=576, d_v=512, Nq=1),                        # latent shape needs v == k
-    dict(d_qk=576, d_v=512, Nq=1, Hq=256, Hkv=1, v_ptr=P * 2),   # > 128 heads per KV head
+    dict(d_qk=576, d_v=512, Nq=2),                        # latent prefill needs v == k
+    dict(d_qk=576, d_v=512, Nq=1),                        # latent decode needs v == k
+    dict(d_qk=576, d_v=512, Nq=64, causal=1, v_ptr=P * 3),   # a separate V is not the latent layout
 ])
 def test_unsupported_shapes(lib, bad):
     assert call(**bad) == gb.ATTN_ERR_UNSUPPORTED

@@ -60,6 +60,19 @@ SMALL = [
     # one long sequence: every output row merges more than 32 split partials
     W("decode_one_long_sequence", B=1, Hq=16, Hkv=1, Nq=1, Nkv=100000, d_qk=576, d_v=512, causal=False,
       scale=1 / math.sqrt(192), v_aliases_k=True),
+    # the latent shape with Nq > 1: the same kernel in prefill mode
+    W("latent_prefill_causal", B=1, Hq=3, Hkv=1, Nq=300, Nkv=300, d_qk=576, d_v=512, causal=True,
+      scale=1 / math.sqrt(192), v_aliases_k=True),
+    W("latent_prefill_rect", B=2, Hq=2, Hkv=2, Nq=130, Nkv=200, d_qk=576, d_v=512, causal=False,
+      scale=1 / math.sqrt(192), v_aliases_k=True),
+    # causal with Nq > Nkv: the first query blocks see no key (O = 0, LSE = -inf)
+    W("latent_prefill_nq_gt_nkv", B=1, Hq=2, Hkv=1, Nq=300, Nkv=129, d_qk=576, d_v=512, causal=True,
+      scale=1 / math.sqrt(192), v_aliases_k=True),
+    W("latent_prefill_zero_scale", B=1, Hq=1, Hkv=1, Nq=200, Nkv=200, d_qk=576, d_v=512, causal=True,
+      scale=0.0, v_aliases_k=True),
+    # one query but 256 query heads per KV head: more rows than a decode tile, so prefill mode
+    W("latent_one_query_many_heads", B=1, Hq=256, Hkv=1, Nq=1, Nkv=200, d_qk=576, d_v=512, causal=False,
+      scale=1 / math.sqrt(192), v_aliases_k=True),
 ]
 
 
@@ -117,6 +130,22 @@ def test_workload_decode_full_size_sampled():
         o_ref, lse_ref = attention_head(q[b, h], k[b, 0], k[b, 0, :, :512], False, wl.scale)
         check(o[b, h], lse[b, h], o_ref, lse_ref, "decode b=%d h=%d" % (b, h))
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
+def test_workload_mla_prefill_full_size_sampled():
+    wl = syn.WORKLOADS["mla_prefill_causal"]
+    inp = syn.make_inputs(wl)
+    o, lse = run_gpu(inp)
+    o = o.cpu().numpy()
+    lse = lse.cpu().numpy()
+    q, k, v = inp.f64()
+    rows = sampled_rows(wl.Nq)
+    for h in (0, 1, wl.Hq // 2, wl.Hq - 1):
+        o_ref, lse_ref = attention_rows(q, k, v, True, wl.scale, 0, h, rows)
+        check(o[0, h, rows], lse[0, h, rows], o_ref, lse_ref, "mla prefill h=%d" % h)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    # causal row 0 attends only to key 0: O = V[0] = K[0, :512]
+    assert np.max(np.abs(o[0, :, 0, :] - v[0, 0, 0, :])) <= 1e-2
 
 
 def test_deterministic_and_nondefault_stream():
