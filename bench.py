@@ -386,11 +386,14 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size (profiling cases)")
+    ap.add_argument("--heads", type=int, default=None, help="override the workload's query heads (profiling cases)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)      # at least three untimed warm-up steps
     wl = syn.WORKLOADS[args.workload]
     if args.batch is not None:
         wl = wl.with_sizes(B=args.batch, name="%s_B%d" % (wl.name, args.batch))
+    if args.heads is not None:
+        wl = wl.with_sizes(Hq=args.heads, name="%s_H%d" % (wl.name, args.heads))
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)
