@@ -353,7 +353,7 @@ def run_ours(args, wl):
         achieved = wl.algorithmic_bytes / per_launch / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_src + " hbm_gbs",
-                "kernel": "decode_kernel + combine_kernel (one step)",
+                "kernel": "latent_kernel (decode mode) + combine_kernel (one step)",
                 "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
                 "tensor_tflops": flops / per_launch / 1e12}
     roof["traffic"] = committed_traffic(kind, wl.name)
