@@ -70,7 +70,7 @@ constexpr uint32_t OFF_A = OFF_Q + QS_BYTES;
 constexpr uint32_t OFF_B = OFF_A + AS * A_BYTES;
 constexpr uint32_t OFF_BAR = OFF_B + BS * B_BYTES;
 constexpr int B_QFULL = 0, B_QEMPTY = 1, B_QTFULL = 2, B_AFULL = 3, B_AEMPTY = B_AFULL + AS, B_BFULL = B_AEMPTY + AS,
-              B_BEMPTY = B_BFULL + BS, B_SFULL = B_BEMPTY + BS, B_PFULL = B_SFULL + 1, B_OFULL = B_PFULL + 1,
+              B_BEMPTY = B_BFULL + BS, B_SFULL = B_BEMPTY + BS, B_PFULL = B_SFULL + 1, B_PHALF = B_PFULL + 1, B_OFULL = B_PHALF + 1,
               B_OEMPTY = B_OFULL + 1, B_DRAIN = B_OEMPTY + 1, NUM_BARS = B_DRAIN + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_SFULL), 1);
     mbar_init(bar(B_PFULL), 4);
+    mbar_init(bar(B_PHALF), 4);
     mbar_init(bar(B_OFULL), 1);
     mbar_init(bar(B_OEMPTY), 4);
     mbar_init(bar(B_DRAIN), 1);
@@ -338,19 +339,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_warp(bar(B_AEMPTY + as));
         if (++as == AS) { as = 0; aph ^= 1u; }
         if (j == S.n - 1) mma_commit_warp(bar(B_QEMPTY));
-        // O += P V: P (64 keys, bf16 pairs) from TMEM over S, V = ring B
-        if (!(ok = warp_wait(bar(B_PFULL), pph, wctx))) break;
-        pph ^= 1u;
+        // O += P V: P (64 keys, bf16 pairs) from TMEM over S, V = ring B;
+        // keys 0..31 as soon as their P is in TMEM, keys 32..63 after
         if (j == 0) {
           // the previous segment's epilogue must have read O
           if (!(ok = warp_wait(bar(B_OEMPTY), oeph ^ 1u, wctx))) break;
           oeph ^= 1u;
         }
+        if (!(ok = warp_wait(bar(B_PHALF), pph, wctx))) break;
         tc_fence_after();
         const uint64_t vd = v_desc0 + ((bs * B_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
+        for (int kk = 0; kk < BN / 32; ++kk)
           mma_ts_warp(dO, dS + kk * 8, vd + ((kk * 16 * 128) >> 4), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        if (!(ok = warp_wait(bar(B_PFULL), pph, wctx))) break;
+        pph ^= 1u;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = BN / 32; kk < BN / 16; ++kk)
+          mma_ts_warp(dO, dS + kk * 8, vd + ((kk * 16 * 128) >> 4), IDESC_PV, 1u);
         mma_commit_warp(bar(B_BEMPTY + bs));
         if (++bs == BS) { bs = 0; bph ^= 1u; }
       }
@@ -479,22 +486,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t c2 = f2_pack(csl, csl);
         const uint64_t nb2 = f2_pack(-base, -base);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-        uint32_t pk[BN / 2];
+        // P in two halves: keys 0..31 are published first, so the MMA warp
+        // starts P V on them while keys 32..63 are computed.
 #pragma unroll
-        for (int i = 0; i < BN / 2; ++i) {
-          const uint64_t x = f2_fma(f2_pack(v[2 * i], v[2 * i + 1]), c2, nb2);
-          const float p0 = ex2(f2_lo(x));
-          const float p1 = ex2(f2_hi(x));
-          acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[BN / 4];
+#pragma unroll
+          for (int i = 0; i < BN / 4; ++i) {
+            const int e = h * (BN / 4) + i;
+            const uint64_t x = f2_fma(f2_pack(v[2 * e], v[2 * e + 1]), c2, nb2);
+            const float p0 = ex2(f2_lo(x));
+            const float p1 = ex2(f2_hi(x));
+            acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tm + lane_addr + COL_S + h * (BN / 4), pk);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(h == 0 ? B_PHALF : B_PFULL));
         }
-        tmem_st32u(tm + lane_addr + COL_S, pk);
         const uint64_t a01 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
         l += f2_lo(a01) + f2_hi(a01);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PFULL));
       }
       if (!ok) break;
       // The next segment's Q first, so that its first Q K^T overlaps this
