@@ -223,12 +223,28 @@ def run_reference(args, wl):
     return 0
 
 
+# O is written as fp32 (attn_fwd, the measured configuration) unless
+# --out bf16 selects attn_fwd_bf16out.
+O_DTYPE = "fp32"
+
+
+def o_torch_dtype():
+    import torch
+    return torch.bfloat16 if O_DTYPE == "bf16" else torch.float32
+
+
+def algorithmic_bytes(wl) -> int:
+    """Workload bytes with O in the selected output type."""
+    o32 = wl.B * wl.Hq * wl.Nq * wl.d_v * 4
+    return wl.algorithmic_bytes - (o32 // 2 if O_DTYPE == "bf16" else 0)
+
+
 def workload_config(wl):
     return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "Nq": wl.Nq, "Nkv": wl.Nkv,
             "d_qk": wl.d_qk, "d_v": wl.d_v, "causal": wl.causal, "scale": wl.scale,
             "inputs": "seeded N(0,1) bf16 (q x%g, k/v x%g)" % (wl.q_factor, wl.kv_factor),
             "l2": "flushed (256 MB write) before every step, outside the step events",
-            "parallelism": "replicas"}
+            "parallelism": "replicas", "o_dtype": O_DTYPE}
 
 
 def measure_device(wl, steps, warmup, world, stream, flush, inputs):
@@ -236,7 +252,7 @@ def measure_device(wl, steps, warmup, world, stream, flush, inputs):
     import torch
     import blackwell_programming_gb300 as gb
     q, k, v = inputs
-    o = torch.empty((wl.B, wl.Hq, wl.Nq, wl.d_v), dtype=torch.float32, device="cuda")
+    o = torch.empty((wl.B, wl.Hq, wl.Nq, wl.d_v), dtype=o_torch_dtype(), device="cuda")
     lse = torch.empty((wl.B, wl.Hq, wl.Nq), dtype=torch.float32, device="cuda")
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -265,7 +281,7 @@ def measure_e2e(wl, steps, warmup, stream, host):
     dq = torch.empty_like(hq, device="cuda")
     dk = torch.empty_like(hk, device="cuda")
     dv = torch.empty_like(hv, device="cuda") if hv is not None else None
-    ho = torch.empty((wl.B, wl.Hq, wl.Nq, wl.d_v), dtype=torch.float32).pin_memory()
+    ho = torch.empty((wl.B, wl.Hq, wl.Nq, wl.d_v), dtype=o_torch_dtype()).pin_memory()
     hl = torch.empty((wl.B, wl.Hq, wl.Nq), dtype=torch.float32).pin_memory()
     o = torch.empty_like(ho, device="cuda")
     lse = torch.empty_like(hl, device="cuda")
@@ -350,13 +366,13 @@ def run_ours(args, wl):
                 "frac": achieved / peaks["bf16_tflops"], "peak_source": peak_src + " bf16_tflops (burst)",
                 "kernel": kname, "algorithmic_flops_per_launch": flops}
     else:
-        achieved = wl.algorithmic_bytes / per_launch / 1e9
+        achieved = algorithmic_bytes(wl) / per_launch / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_src + " hbm_gbs",
                 "kernel": "latent_kernel (decode mode) + combine_kernel (one step)",
-                "algorithmic_bytes_per_launch": wl.algorithmic_bytes,
+                "algorithmic_bytes_per_launch": algorithmic_bytes(wl),
                 "tensor_tflops": flops / per_launch / 1e12}
-    roof["traffic"] = committed_traffic(kind, wl.name)
+    roof["traffic"] = committed_traffic(kind, wl.name) if O_DTYPE == "fp32" else None
     launches = (2 if kind == "decode" else 1) * args.steps
 
     if rank == 0:
@@ -387,8 +403,11 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size (profiling cases)")
     ap.add_argument("--heads", type=int, default=None, help="override the workload's query heads (profiling cases)")
+    ap.add_argument("--out", default="fp32", choices=["fp32", "bf16"], help="O output type (fp32 is the measured configuration)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)      # at least three untimed warm-up steps
+    global O_DTYPE
+    O_DTYPE = args.out
     wl = syn.WORKLOADS[args.workload]
     if args.batch is not None:
         wl = wl.with_sizes(B=args.batch, name="%s_B%d" % (wl.name, args.batch))

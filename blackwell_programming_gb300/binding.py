@@ -22,7 +22,7 @@ ATTN_ERR_NO_DEVICE = 5
 ATTN_ERR_SCRATCH_LIMIT = 6
 
 # Symbols the shared library exports (the declarations of include/gbattn.h).
-EXPORTS = ("attn_fwd", "attn_check_device", "attn_status_string", "attn_last_cuda_error",
+EXPORTS = ("attn_fwd", "attn_fwd_bf16out", "attn_check_device", "attn_status_string", "attn_last_cuda_error",
            "attn_version", "attn_decode_workspace_bytes", "attn_decode_fwd_noalloc")
 
 _lib = None
@@ -47,6 +47,8 @@ def load_library(path: str | None = None):
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
     L.attn_fwd.restype = i
+    L.attn_fwd_bf16out.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
+    L.attn_fwd_bf16out.restype = i
     L.attn_check_device.argtypes = [vp, i]
     L.attn_check_device.restype = i
     L.attn_status_string.argtypes = [i]
@@ -128,15 +130,17 @@ def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B
 
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-             want_lse: bool = True, stream=None):
+             want_lse: bool = True, stream=None, out_dtype=None):
     """O = softmax(mask(scale * Q K^T)) V and LSE on the GPU.
 
     q: bf16 [B, Hq, Nq, d_qk]; k: bf16 [B, Hkv, Nkv, d_qk];
     v: bf16 [B, Hkv, Nkv, d_v], or the view ``k[..., :d_v]`` of k (the latent
     layout where V is the first d_v features of K).  All on one CUDA device,
     contiguous (a view of k is accepted for v as described).  scale defaults
-    to 1/sqrt(d_qk).  Returns (o fp32 [B, Hq, Nq, d_v], lse fp32 [B, Hq, Nq]
-    or None).  Work is queued on ``stream`` (default: the current stream).
+    to 1/sqrt(d_qk).  Returns (o [B, Hq, Nq, d_v], lse fp32 [B, Hq, Nq] or
+    None).  O is fp32 (attn_fwd), or bf16 when ``out_dtype`` is
+    torch.bfloat16 or ``out`` is a bf16 tensor (attn_fwd_bf16out).  Work is
+    queued on ``stream`` (default: the current stream).
     """
     import torch
     L = load_library()
@@ -164,21 +168,26 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
     if scale is None:
         scale = 1.0 / math.sqrt(d_qk)
     dev = q.device
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.float32
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("O is fp32 or bf16, not %s" % out_dtype)
     if out is None:
-        out = torch.empty((B, Hq, Nq, d_v), dtype=torch.float32, device=dev)
-    elif out.shape != (B, Hq, Nq, d_v) or out.dtype != torch.float32 or not out.is_contiguous() or out.device != dev:
-        raise ValueError("out must be a contiguous fp32 [B, Hq, Nq, d_v] tensor on q's device")
+        out = torch.empty((B, Hq, Nq, d_v), dtype=out_dtype, device=dev)
+    elif out.shape != (B, Hq, Nq, d_v) or out.dtype != out_dtype or not out.is_contiguous() or out.device != dev:
+        raise ValueError("out must be a contiguous %s [B, Hq, Nq, d_v] tensor on q's device" % out_dtype)
     if want_lse and lse is None:
         lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
     elif lse is not None and (lse.shape != (B, Hq, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
         raise ValueError("lse must be a contiguous fp32 [B, Hq, Nq] tensor")
     v_ptr = k.data_ptr() if aliased else v.data_ptr()
+    fn = L.attn_fwd if out_dtype == torch.float32 else L.attn_fwd_bf16out
     with torch.cuda.device(dev):
-        st = L.attn_fwd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v_ptr),
+        st = fn(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v_ptr),
                         ctypes.c_void_p(out.data_ptr()),
                         ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
                         B, Hq, Hkv, Nq, Nkv, d_qk, d_v, 1 if causal else 0, ctypes.c_float(scale),
                         _stream_handle(stream, dev))
     if st != ATTN_OK:
-        _raise(L, st, "attn_fwd")
+        _raise(L, st, fn.__name__)
     return out, lse

@@ -189,9 +189,15 @@ int attn_check_device(attn_stream_t stream, int reset) {
   return read_device_error(reinterpret_cast<cudaStream_t>(stream), d->err, reset);
 }
 
-int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq, int Hkv, int Nq,
-             int Nkv, int d_qk, int d_v, int causal, float scale, attn_stream_t stream_) {
+}  // extern "C"
+
+namespace {
+
+// attn_fwd and attn_fwd_bf16out: O is written as fp32 (o32) or bf16 (o16).
+int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint16_t* o16, float* lse, int B, int Hq,
+                  int Hkv, int Nq, int Nkv, int d_qk, int d_v, int causal, float scale, attn_stream_t stream_) {
   t_cuda_error[0] = '\0';
+  const void* o = o32 != nullptr ? static_cast<const void*>(o32) : static_cast<const void*>(o16);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   // ---------------------------------------------------------------- checks
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
@@ -229,7 +235,8 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, 
     if ((st = make_map(&tk, k, d, Nkv, static_cast<uint64_t>(B) * Hkv, rs, rs * Nkv, 128)) != ATTN_OK) return st;
     if ((st = make_map(&tv, v, d, Nkv, static_cast<uint64_t>(B) * Hkv, rs, rs * Nkv, 128)) != ATTN_OK) return st;
     PrefillParams p{};
-    p.o = o;
+    p.o = o32;
+    p.o_bf16 = o16;
     p.lse = lse;
     p.B = B;
     p.Hq = Hq;
@@ -254,7 +261,8 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, 
       return st;
     LatentPrefillParams p{};
     p.q = static_cast<const uint16_t*>(q);
-    p.o = o;
+    p.o = o32;
+    p.o_bf16 = o16;
     p.lse = lse;
     p.B = B;
     p.Hq = Hq;
@@ -297,7 +305,7 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, 
       cudaFreeAsync(ws, stream);
       return cuda_fail(e, "decode launch");
     }
-    if ((e = launch_combine(p, grid, o, lse, stream)) != cudaSuccess) {
+    if ((e = launch_combine(p, grid, o32, o16, lse, stream)) != cudaSuccess) {
       cudaFreeAsync(ws, stream);
       return cuda_fail(e, "combine launch");
     }
@@ -306,6 +314,22 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, 
 
   if (check_env()) return read_device_error(stream, dev->err, 0);
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq, int Hkv, int Nq,
+             int Nkv, int d_qk, int d_v, int causal, float scale, attn_stream_t stream) {
+  return attn_fwd_impl(q, k, v, o, nullptr, lse, B, Hq, Hkv, Nq, Nkv, d_qk, d_v, causal, scale, stream);
+}
+
+int attn_fwd_bf16out(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nkv, int d_qk, int d_v, int causal, float scale, attn_stream_t stream) {
+  if (o == nullptr) return ATTN_ERR_INVALID_ARG;
+  return attn_fwd_impl(q, k, v, nullptr, static_cast<uint16_t*>(o), lse, B, Hq, Hkv, Nq, Nkv, d_qk, d_v, causal,
+                       scale, stream);
 }
 
 }  // extern "C"
@@ -396,7 +420,7 @@ extern "C" int attn_decode_fwd_noalloc(const void* q, const void* kv, float* o, 
   p.lse_part = scratch + n_slots * 256;
   cudaError_t e;
   if ((e = launch_decode(tq, tk, p, grid, stream)) != cudaSuccess) return cuda_fail(e, "decode launch");
-  if ((e = launch_combine(p, grid, o, lse, stream)) != cudaSuccess) return cuda_fail(e, "combine launch");
+  if ((e = launch_combine(p, grid, o, nullptr, lse, stream)) != cudaSuccess) return cuda_fail(e, "combine launch");
   if (check_env()) return read_device_error(stream, dev->err, 0);
   return ATTN_OK;
 }

@@ -410,9 +410,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (s.n > 0) return true;
         if constexpr (kPrefill) {
           if (q_live(p, s, r)) {
-            float* orow = p.o + (static_cast<size_t>(s.qplane) * p.Nq + s.qrow0 + r) * (2 * DVH) + s.half * DVH;
+            const size_t orow = (static_cast<size_t>(s.qplane) * p.Nq + s.qrow0 + r) * (2 * DVH) + s.half * DVH;
+            if (p.o_bf16 != nullptr) {
 #pragma unroll 4
-            for (int c = 0; c < DVH / 4; ++c) reinterpret_cast<float4*>(orow)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int c = 0; c < DVH / 8; ++c) reinterpret_cast<uint4*>(p.o_bf16 + orow)[c] = make_uint4(0u, 0u, 0u, 0u);
+            } else {
+#pragma unroll 4
+              for (int c = 0; c < DVH / 4; ++c) reinterpret_cast<float4*>(p.o + orow)[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
             if (s.half == 0 && p.lse != nullptr) p.lse[static_cast<size_t>(s.qplane) * p.Nq + s.qrow0 + r] = -INFINITY;
           }
         }
@@ -523,27 +528,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // O half of rows qrow0 .. qrow0+127, straight to the output.  O
         // leaves TMEM in the 16x256b shape, so each warp store writes 8 rows
         // x 32 contiguous bytes.
-        float* ohead = p.o + (static_cast<size_t>(S.qplane) * p.Nq) * (2 * DVH) + S.half * DVH;
+        const size_t ohead = (static_cast<size_t>(S.qplane) * p.Nq) * (2 * DVH) + S.half * DVH;
+        const bool bf = p.o_bf16 != nullptr;
 #pragma unroll 1
         for (int hl = 0; hl < 2; ++hl) {
           const int ra = static_cast<int>(warp * 32 + hl * 16 + (lane >> 2));   // rows ra and ra + 8 of the tile
           const float ia = __shfl_sync(kFull, inv_l, hl * 16 + (lane >> 2));
           const float ib = __shfl_sync(kFull, inv_l, hl * 16 + (lane >> 2) + 8);
           const bool la = S.qrow0 + ra < p.Nq, lb = S.qrow0 + ra + 8 < p.Nq;
-          float* oa = ohead + static_cast<size_t>(la ? S.qrow0 + ra : 0) * (2 * DVH) + 2 * (lane & 3);
-          float* ob = ohead + static_cast<size_t>(lb ? S.qrow0 + ra + 8 : 0) * (2 * DVH) + 2 * (lane & 3);
+          const size_t oa = ohead + static_cast<size_t>(la ? S.qrow0 + ra : 0) * (2 * DVH) + 2 * (lane & 3);
+          const size_t ob = ohead + static_cast<size_t>(lb ? S.qrow0 + ra + 8 : 0) * (2 * DVH) + 2 * (lane & 3);
 #pragma unroll 1
           for (int ch = 0; ch < DVH / 64; ++ch) {
             uint32_t rr[32];
             tmem_ld16x256b_x8(tm + ((warp * 32u + hl * 16u) << 16) + COL_O + ch * 64, rr);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              if (la)
-                *reinterpret_cast<float2*>(oa + ch * 64 + 8 * k) =
-                    make_float2(__uint_as_float(rr[4 * k]) * ia, __uint_as_float(rr[4 * k + 1]) * ia);
-              if (lb)
-                *reinterpret_cast<float2*>(ob + ch * 64 + 8 * k) =
-                    make_float2(__uint_as_float(rr[4 * k + 2]) * ib, __uint_as_float(rr[4 * k + 3]) * ib);
+              const float a0 = __uint_as_float(rr[4 * k]) * ia, a1 = __uint_as_float(rr[4 * k + 1]) * ia;
+              const float b0 = __uint_as_float(rr[4 * k + 2]) * ib, b1 = __uint_as_float(rr[4 * k + 3]) * ib;
+              const size_t c = static_cast<size_t>(ch * 64 + 8 * k);
+              if (bf) {
+                if (la) *reinterpret_cast<uint32_t*>(p.o_bf16 + oa + c) = pack_bf16x2(a0, a1);
+                if (lb) *reinterpret_cast<uint32_t*>(p.o_bf16 + ob + c) = pack_bf16x2(b0, b1);
+              } else {
+                if (la) *reinterpret_cast<float2*>(p.o + oa + c) = make_float2(a0, a1);
+                if (lb) *reinterpret_cast<float2*>(p.o + ob + c) = make_float2(b0, b1);
+              }
             }
           }
         }
@@ -593,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // partials are.
 constexpr int kCombineWarps = 4;
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecodeParams p, int grid, float* o,
-                                                                     float* lse) {
+                                                                     uint16_t* o_bf16, float* lse) {
   __shared__ float tile[kCombineWarps][32][33];
   const int wib = static_cast<int>(threadIdx.x >> 5);
   const int wid = blockIdx.x * kCombineWarps + wib;
@@ -638,7 +648,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
     }
   }
   const float inv = (tot > 0.f) ? 1.f / tot : 0.f;
-  float* out_rows = o + (static_cast<size_t>(plane) * p.group + r0) * (2 * DVH) + half * DVH;
+  const size_t out_rows = (static_cast<size_t>(plane) * p.group + r0) * (2 * DVH) + half * DVH;
   float4 acc[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -665,8 +675,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
     tile[wib][lane][4 * c + 3] = acc[c].w;
   }
   __syncwarp();
-  for (int row = 0; row < 32 && r0 + row < p.group; ++row)
-    out_rows[static_cast<size_t>(row) * (2 * DVH) + blk * 32 + lane] = tile[wib][row][lane];
+  for (int row = 0; row < 32 && r0 + row < p.group; ++row) {
+    const size_t at = out_rows + static_cast<size_t>(row) * (2 * DVH) + blk * 32 + lane;
+    if (o != nullptr)
+      o[at] = tile[wib][row][lane];
+    else
+      o_bf16[at] = static_cast<uint16_t>(pack_bf16x2(tile[wib][row][lane], 0.f) & 0xFFFFu);   // round to nearest even
+  }
   if (half == 0 && blk == 0 && live && lse != nullptr)
     lse[static_cast<size_t>(plane) * p.group + r] = (tot > 0.f) ? mx + logf(tot) : -INFINITY;
 }
@@ -708,9 +723,11 @@ cudaError_t launch_latent_prefill(const CUtensorMap& tq, const CUtensorMap& tk, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const DecodeParams& p, int grid, float* o, float* lse, cudaStream_t stream) {
+cudaError_t launch_combine(const DecodeParams& p, int grid, float* o, uint16_t* o_bf16, float* lse,
+                           cudaStream_t stream) {
   const int warps = 2 * p.planes * ((p.group + 31) / 32) * (DVH / 32);
-  combine_kernel<<<(warps + kCombineWarps - 1) / kCombineWarps, kCombineWarps * 32, 0, stream>>>(p, grid, o, lse);
+  combine_kernel<<<(warps + kCombineWarps - 1) / kCombineWarps, kCombineWarps * 32, 0, stream>>>(p, grid, o, o_bf16,
+                                                                                                    lse);
   return cudaGetLastError();
 }
 

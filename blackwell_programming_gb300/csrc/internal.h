@@ -11,7 +11,8 @@ namespace gbattn {
 // Prefill: one persistent CTA per SM walks "units" of two 128-row query
 // tiles of one (batch, head) pair.
 struct PrefillParams {
-  float* o;
+  float* o;            // fp32 O, or null when o_bf16 is set
+  uint16_t* o_bf16;    // bf16 O (same layout), or null
   float* lse;          // may be null
   int B, Hq, Hkv, Nq, Nkv, d_v;
   int causal;
@@ -46,7 +47,8 @@ struct DecodeParams {
 // work item writes its half of O and (half 0) the LSE directly.
 struct LatentPrefillParams {
   const uint16_t* q;   // bf16 Q [B * Hq, Nq, 576]
-  float* o;            // fp32 O [B * Hq, Nq, 512]
+  float* o;            // fp32 O [B * Hq, Nq, 512], or null when o_bf16 is set
+  uint16_t* o_bf16;    // bf16 O (same layout), or null
   float* lse;          // fp32 LSE [B * Hq, Nq], may be null
   int B, Hq, Hkv, Nq, Nkv;
   int causal;
@@ -68,7 +70,9 @@ int decode_key_tile();   // keys per K tile of the decode kernel (TMA box rows)
 cudaError_t launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const DecodeParams& p, int grid,
                           cudaStream_t stream);
 
-// Merge the partials of every row into O [planes * group, 512] and LSE.
-cudaError_t launch_combine(const DecodeParams& p, int grid, float* o, float* lse, cudaStream_t stream);
+// Merge the partials of every row into O [planes * group, 512] and LSE; O is
+// fp32 (o) or, when o is null, bf16 (o_bf16).
+cudaError_t launch_combine(const DecodeParams& p, int grid, float* o, uint16_t* o_bf16, float* lse,
+                           cudaStream_t stream);
 
 }  // namespace gbattn

@@ -472,15 +472,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O leaves TMEM in the 16x256b shape: each store instruction of the
       // warp then writes 8 rows x 32 contiguous bytes (whole sectors),
       // instead of 32 rows x 16 bytes with one row per thread.
-      float* ohead = p.o + static_cast<size_t>(U.b * p.Hq + U.h) * p.Nq * D;
+      // fp32 O, or bf16 O when the call asked for it (p.o_bf16)
+      const size_t ohead = static_cast<size_t>(U.b * p.Hq + U.h) * p.Nq * D;
+      const bool bf = p.o_bf16 != nullptr;
 #pragma unroll 1
       for (int hl = 0; hl < 2; ++hl) {
         const int ra = static_cast<int>(quad * 32 + hl * 16 + (lane >> 2));   // rows ra and ra + 8 of the tile
         const float ia = __shfl_sync(kFull, inv_l, hl * 16 + (lane >> 2));
         const float ib = __shfl_sync(kFull, inv_l, hl * 16 + (lane >> 2) + 8);
         const bool la = q0 + ra < p.Nq, lb = q0 + ra + 8 < p.Nq;
-        float* oa = ohead + static_cast<size_t>(la ? q0 + ra : 0) * D + 2 * (lane & 3);
-        float* ob = ohead + static_cast<size_t>(lb ? q0 + ra + 8 : 0) * D + 2 * (lane & 3);
+        const size_t oa = ohead + static_cast<size_t>(la ? q0 + ra : 0) * D + 2 * (lane & 3);
+        const size_t ob = ohead + static_cast<size_t>(lb ? q0 + ra + 8 : 0) * D + 2 * (lane & 3);
 #pragma unroll 1
         for (int ch = 0; ch < D / 64; ++ch) {
           uint32_t r[32];
@@ -492,12 +494,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            if (la)
-              *reinterpret_cast<float2*>(oa + ch * 64 + 8 * k) =
-                  make_float2(__uint_as_float(r[4 * k]) * ia, __uint_as_float(r[4 * k + 1]) * ia);
-            if (lb)
-              *reinterpret_cast<float2*>(ob + ch * 64 + 8 * k) =
-                  make_float2(__uint_as_float(r[4 * k + 2]) * ib, __uint_as_float(r[4 * k + 3]) * ib);
+            const float a0 = __uint_as_float(r[4 * k]) * ia, a1 = __uint_as_float(r[4 * k + 1]) * ia;
+            const float b0 = __uint_as_float(r[4 * k + 2]) * ib, b1 = __uint_as_float(r[4 * k + 3]) * ib;
+            const size_t c = static_cast<size_t>(ch * 64 + 8 * k);
+            if (bf) {
+              if (la) *reinterpret_cast<uint32_t*>(p.o_bf16 + oa + c) = pack_bf16x2(a0, a1);
+              if (lb) *reinterpret_cast<uint32_t*>(p.o_bf16 + ob + c) = pack_bf16x2(b0, b1);
+            } else {
+              if (la) *reinterpret_cast<float2*>(p.o + oa + c) = make_float2(a0, a1);
+              if (lb) *reinterpret_cast<float2*>(p.o + ob + c) = make_float2(b0, b1);
+            }
           }
         }
       }

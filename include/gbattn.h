@@ -93,6 +93,17 @@ int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse,
              int causal, float scale, attn_stream_t stream);
 
 /*
+ * attn_fwd_bf16out - attn_fwd with O written as bf16 (round to nearest even)
+ * instead of fp32: same arguments, layouts, supported shapes, LSE (fp32) and
+ * errors, with o a bf16 [B, Hq, Nq, d_v] buffer (16-byte aligned).  It
+ * halves O's share of the HBM traffic; the arithmetic is unchanged (fp32
+ * accumulation, one rounding of each normalised output).
+ */
+int attn_fwd_bf16out(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int Nq, int Nkv, int d_qk, int d_v,
+                     int causal, float scale, attn_stream_t stream);
+
+/*
  * attn_check_device - synchronise `stream` and read the device error word
  * that the kernels set when a bounded wait gives up (see
  * ATTN_ERR_TIMEOUT).  reset != 0 clears the word.  Returns ATTN_OK,

@@ -206,3 +206,34 @@ def test_lse_optional():
 def test_error_word_clear_after_runs():
     import blackwell_programming_gb300 as gb
     assert gb.attn_check_device(reset=True) == 0
+
+
+BF16_OUT = [
+    W("bf16o_d128_causal", B=1, Hq=4, Hkv=2, Nq=300, Nkv=300, d_qk=128, d_v=128, causal=True, scale=0.088),
+    W("bf16o_d64_rect", B=2, Hq=2, Hkv=1, Nq=77, Nkv=300, d_qk=64, d_v=64, causal=False, scale=0.125),
+    W("bf16o_nq_gt_nkv", B=1, Hq=2, Hkv=1, Nq=300, Nkv=129, d_qk=128, d_v=128, causal=True, scale=0.088),
+    W("bf16o_latent_prefill", B=1, Hq=3, Hkv=1, Nq=300, Nkv=300, d_qk=576, d_v=512, causal=True,
+      scale=1 / math.sqrt(192), v_aliases_k=True),
+    W("bf16o_decode", B=2, Hq=16, Hkv=1, Nq=1, Nkv=700, d_qk=576, d_v=512, causal=False,
+      scale=1 / math.sqrt(192), v_aliases_k=True),
+]
+
+
+@pytest.mark.parametrize("wl", BF16_OUT, ids=lambda w: w.name)
+def test_bf16_output(wl):
+    """attn_fwd_bf16out: within the same tolerance of the oracle, and equal bit for bit to the fp32
+    output rounded to bf16 (the kernel rounds each normalised fp32 value once, to nearest even)."""
+    import blackwell_programming_gb300 as gb
+    inp = syn.make_inputs(wl)
+    q, k, v = to_torch(inp)
+    gb.attn_check_device(reset=True)
+    o16, lse16 = gb.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, out_dtype=torch.bfloat16)
+    o32, lse32 = gb.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale)
+    torch.cuda.synchronize()
+    assert gb.attn_check_device(reset=True) == 0
+    assert o16.dtype == torch.bfloat16 and o16.shape == o32.shape
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.equal(lse16, lse32)
+    qf, kf, vf = inp.f64()
+    o_ref, lse_ref = attention(qf, kf, vf, wl.causal, wl.scale)
+    check(o16.float().cpu().numpy(), lse16.cpu().numpy(), o_ref, lse_ref, wl.name)
