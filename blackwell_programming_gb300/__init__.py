@@ -1,8 +1,9 @@
 """Fused attention forward for one NVIDIA GB300 (sm_103a).
 
 The compute path is libgbattn.so (hand-written CUDA with tcgen05, TMA and
-mbarrier inline PTX) behind the C ABI of include/gbattn.h; this package is a
-thin ctypes binding over it plus the seeded synthetic-input generator.
+mbarrier inline PTX) behind the C ABI of include/gbattn.h (attention) and
+include/gbgemm.h (the projection GEMM around it); this package is a thin
+ctypes binding over it plus the seeded synthetic-input generator.
 """
 from . import _build
 from .binding import (ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG, ATTN_ERR_NO_DEVICE, ATTN_ERR_SCRATCH_LIMIT,
@@ -10,7 +11,7 @@ from .binding import (ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG, ATTN_ERR_NO_DEVICE, A
                       attn_check_device, attn_decode_fwd_noalloc,
                       attn_decode_workspace_bytes, attn_fwd, attn_fwd_raw, attn_last_cuda_error,
                       attn_status_string,
-                      attn_version, load_library)
+                      attn_version, gemm_nt, gemm_raw, load_library)
 
 
 def build(force: bool = False) -> str:
@@ -23,4 +24,5 @@ def build(force: bool = False) -> str:
 __all__ = ["build", "attn_fwd", "attn_fwd_raw", "attn_check_device", "attn_status_string",
            "attn_version", "attn_decode_workspace_bytes", "attn_last_cuda_error", "AttnError", "load_library", "EXPORTS",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
-           "ATTN_ERR_TIMEOUT", "ATTN_ERR_NO_DEVICE", "ATTN_ERR_SCRATCH_LIMIT", "attn_decode_fwd_noalloc"]
+           "ATTN_ERR_TIMEOUT", "ATTN_ERR_NO_DEVICE", "ATTN_ERR_SCRATCH_LIMIT", "attn_decode_fwd_noalloc",
+           "gemm_nt", "gemm_raw"]

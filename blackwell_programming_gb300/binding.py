@@ -23,7 +23,7 @@ ATTN_ERR_SCRATCH_LIMIT = 6
 
 # Symbols the shared library exports (the declarations of include/gbattn.h).
 EXPORTS = ("attn_fwd", "attn_fwd_bf16out", "attn_check_device", "attn_status_string", "attn_last_cuda_error",
-           "attn_version", "attn_decode_workspace_bytes", "attn_decode_fwd_noalloc")
+           "attn_version", "attn_decode_workspace_bytes", "attn_decode_fwd_noalloc", "gemm_bf16_nt")
 
 _lib = None
 
@@ -49,6 +49,8 @@ def load_library(path: str | None = None):
     L.attn_fwd.restype = i
     L.attn_fwd_bf16out.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
     L.attn_fwd_bf16out.restype = i
+    L.gemm_bf16_nt.argtypes = [vp, vp, vp, i, i, i, i, vp]
+    L.gemm_bf16_nt.restype = i
     L.attn_check_device.argtypes = [vp, i]
     L.attn_check_device.restype = i
     L.attn_status_string.argtypes = [i]
@@ -127,6 +129,48 @@ def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B
     return L.attn_fwd(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
                       ctypes.c_void_p(o_ptr), ctypes.c_void_p(lse_ptr), B, Hq, Hkv, Nq, Nkv, d_qk, d_v,
                       1 if causal else 0, ctypes.c_float(scale), ctypes.c_void_p(stream_ptr))
+
+
+def gemm_raw(a_ptr: int, b_ptr: int, c_ptr: int, M: int, N: int, K: int, c_fp32: bool,
+             stream_ptr: int = 0) -> int:
+    """The C call gemm_bf16_nt with raw integer pointers; returns the status code."""
+    L = load_library()
+    return L.gemm_bf16_nt(ctypes.c_void_p(a_ptr), ctypes.c_void_p(b_ptr), ctypes.c_void_p(c_ptr), M, N, K,
+                          1 if c_fp32 else 0, ctypes.c_void_p(stream_ptr))
+
+
+def gemm_nt(a, b, out=None, out_dtype=None, stream=None):
+    """C = A B^T on the GPU: a bf16 [M, K], b bf16 [N, K] (a linear layer's
+    weight), both contiguous on one CUDA device; C [M, N] bf16 (default) or
+    fp32.  Work is queued on ``stream`` (default: the current stream)."""
+    import torch
+    L = load_library()
+    for name, t in (("a", a), ("b", b)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2:
+            raise TypeError("%s must be a 2-D bfloat16 CUDA tensor" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    if a.device != b.device:
+        raise ValueError("a and b must be on one device")
+    M, K = a.shape
+    N, Kb = b.shape
+    if Kb != K:
+        raise ValueError("shape mismatch: a %s b %s" % (tuple(a.shape), tuple(b.shape)))
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.bfloat16
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("C is fp32 or bf16, not %s" % out_dtype)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    elif out.shape != (M, N) or out.dtype != out_dtype or not out.is_contiguous() or out.device != a.device:
+        raise ValueError("out must be a contiguous %s [M, N] tensor on a's device" % out_dtype)
+    with torch.cuda.device(a.device):
+        st = L.gemm_bf16_nt(ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()),
+                            ctypes.c_void_p(out.data_ptr()), M, N, K, 1 if out_dtype == torch.float32 else 0,
+                            _stream_handle(stream, a.device))
+    if st != ATTN_OK:
+        _raise(L, st, "gemm_bf16_nt")
+    return out
 
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,

@@ -18,6 +18,7 @@
 #include <cudaTypedefs.h>
 
 #include "gbattn.h"
+#include "gbgemm.h"
 #include "internal.h"
 
 namespace gbattn {
@@ -323,6 +324,38 @@ extern "C" {
 int attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq, int Hkv, int Nq,
              int Nkv, int d_qk, int d_v, int causal, float scale, attn_stream_t stream) {
   return attn_fwd_impl(q, k, v, o, nullptr, lse, B, Hq, Hkv, Nq, Nkv, d_qk, d_v, causal, scale, stream);
+}
+
+int gemm_bf16_nt(const void* a, const void* b, void* c, int M, int N, int K, int c_fp32, attn_stream_t stream_) {
+  t_cuda_error[0] = '\0';
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (a == nullptr || b == nullptr || c == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0 || K % 8 != 0 || N % 2 != 0) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(M) * K >= (1LL << 31) || static_cast<long long>(N) * K >= (1LL << 31) ||
+      static_cast<long long>(M) * N >= (1LL << 31))
+    return ATTN_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  CUtensorMap ta, tb;
+  const uint64_t rs = static_cast<uint64_t>(K) * 2;
+  if ((st = make_map(&ta, a, K, M, 1, rs, rs * M, gemm_tile_rows())) != ATTN_OK) return st;
+  if ((st = make_map(&tb, b, K, N, 1, rs, rs * N, gemm_tile_cols())) != ATTN_OK) return st;
+  GemmParams p{};
+  p.c = c;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.c_fp32 = c_fp32 ? 1 : 0;
+  p.tiles_m = (M + gemm_tile_rows() - 1) / gemm_tile_rows();
+  p.tiles_n = (N + gemm_tile_cols() - 1) / gemm_tile_cols();
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.err = dev->err;
+  cudaError_t e;
+  if ((e = launch_gemm(ta, tb, p, dev->num_sms, stream)) != cudaSuccess) return cuda_fail(e, "gemm launch");
+  if (check_env()) return read_device_error(stream, dev->err, 0);
+  return ATTN_OK;
 }
 
 int attn_fwd_bf16out(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,

@@ -1,0 +1,237 @@
+// gemm_sm103.cu - C = A B^T in bf16 with fp32 accumulation, for the
+// projections that feed and drain the attention forward (the QKV and O
+// projections of the decoder chain on "CS149 L11: Programming Specialized
+// Hardware", section 6; the matrix-multiply kernel of its section 4 is the
+// pages' model: a producer of tiles, a consumer that runs the tensor core, a
+// pipeline of stages between them).
+//
+// A is [M, K] row-major (activations), B is [N, K] row-major (a linear layer's
+// weight), C is [M, N] row-major in bf16 or fp32.
+//
+// How, on sm_103a:
+//  * One persistent CTA per SM walks 128 x 256 output tiles in groups of
+//    kGroupM row blocks (all column blocks of a group before the next group),
+//    so that the A and B tiles a wave of CTAs works on stay in L2.
+//  * Warp 5 is the TMA producer: per 64-deep K step it loads a 128 x 64 A box
+//    and a 256 x 64 B box (128-byte swizzle) into one of kStages ring stages.
+//  * Warp 4 issues tcgen05.mma (M 128, N 256, K 16: four per stage, one elect
+//    each group of four) into one of two 256-column TMEM accumulators, so
+//    that the epilogue of one tile runs while the next tile accumulates.
+//  * Warps 0-3 are the epilogue: each reads its 32 accumulator rows in the
+//    16x256b shape (8 rows x 32 bytes per store instruction of the warp),
+//    converts and stores C, then hands the accumulator back.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 4;
+constexpr int kGroupM = 16;
+constexpr int kThreads = 192;
+constexpr int kMmaWarp = 4;
+constexpr int kTmaWarp = 5;
+constexpr uint32_t kFull = 0xFFFFFFFFu;
+
+constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t OFF_BAR = kStages * STAGE_BYTES;
+constexpr int B_FULL = 0, B_EMPTY = kStages, B_ACCFULL = 2 * kStages, B_ACCEMPTY = B_ACCFULL + 2,
+              B_DRAIN = B_ACCEMPTY + 2, NUM_BARS = B_DRAIN + 1;
+constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alignment
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, false);
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+  const bool ok = mbar_wait(bar, parity, w);
+  return __all_sync(kFull, ok);
+}
+
+// Tile t -> (row block, column block): groups of kGroupM row blocks, the row
+// block fastest inside a group.
+__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb, int& nb) {
+  const int per_group = kGroupM * p.tiles_n;
+  const int g = t / per_group;
+  const int first = g * kGroupM;
+  const int gsize = min(p.tiles_m - first, kGroupM);
+  const int in = t - g * per_group;
+  mb = first + in % gsize;
+  nb = in / gsize;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC + 4);
+  const WaitCtx wctx{abort_flag, p.err};
+  const uint32_t warp = warp_id(), lane = lane_id();
+  const int kblocks = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0u;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(B_FULL + s), 1);
+      mbar_init(bar(B_EMPTY + s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar(B_ACCFULL + a), 1);
+      mbar_init(bar(B_ACCEMPTY + a), 4);
+    }
+    mbar_init(bar(B_DRAIN), 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tmem_slot;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      const uint64_t pol = l2_policy_evict_last();   // tiles are re-read by the other CTAs of a group
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t filled = 0u, fill_par = 0u;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, p, mb, nb);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!(ok = mbar_wait(bar(B_EMPTY + s), ph ^ 1u, wctx))) break;
+          const uint32_t st = sbase + s * STAGE_BYTES;
+          mbar_arrive_expect_tx(bar(B_FULL + s), STAGE_BYTES);
+          filled |= 1u << s;
+          fill_par = (fill_par & ~(1u << s)) | (ph << s);
+          tma_load_3d(st, &tmA, bar(B_FULL + s), kb * BK, mb * BM, 0, pol);
+          tma_load_3d(st + A_BYTES, &tmB, bar(B_FULL + s), kb * BK, nb * BN, 0, pol);
+          if (++s == kStages) { s = 0; ph ^= 1u; }
+        }
+      }
+      // Every issued copy must have landed before the CTA may exit.
+      for (int b = 0; b < kStages; ++b)
+        if ((filled >> b) & 1u) mbar_wait_drain(bar(B_FULL + b), (fill_par >> b) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------ MMA issuer (whole warp)
+    int s = 0;
+    uint32_t ph = 0;
+    uint32_t aeph = 0u;   // bit a: parity of accumulator a's next "empty" wait
+    const uint64_t a_desc0 = smem_desc_sw128(sbase, 16, 1024);
+    const uint64_t b_desc0 = smem_desc_sw128(sbase + A_BYTES, 16, 1024);
+    bool ok = true;
+    int i = 0;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++i) {
+      const int a = i & 1;
+      // the epilogue has read this accumulator's previous tile
+      if (!(ok = warp_wait(bar(B_ACCEMPTY + a), ((aeph >> a) & 1u) ^ 1u, wctx))) break;
+      aeph ^= 1u << a;
+      tc_fence_after();
+      const uint32_t d = tm + a * BN;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!(ok = warp_wait(bar(B_FULL + s), ph, wctx))) break;
+        tc_fence_after();
+        const uint64_t ad = a_desc0 + ((s * STAGE_BYTES) >> 4);
+        const uint64_t bd = b_desc0 + ((s * STAGE_BYTES) >> 4);
+        uint64_t da[4], db[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          da[kk] = ad + kk * 2;   // +32 bytes per 16-deep step inside the 128-byte swizzled row
+          db[kk] = bd + kk * 2;
+        }
+        mma_ss_warp4(d, da, db, IDESC, kb > 0 ? 1u : 0u);
+        mma_commit_warp(bar(B_EMPTY + s));
+        if (++s == kStages) { s = 0; ph ^= 1u; }
+      }
+      if (!ok) break;
+      mma_commit_warp(bar(B_ACCFULL + a));
+    }
+    mma_commit_warp(bar(B_DRAIN));
+    mbar_wait_drain(bar(B_DRAIN), 0);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t quad = warp;   // warps 0-3 own TMEM lanes 32*warp .. +31
+    uint32_t afph = 0u;   // bit a: parity of accumulator a's next "full" wait
+    bool ok = true;
+    int i = 0;
+    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++i) {
+      const int a = i & 1;
+      int mb, nb;
+      tile_coords(t, p, mb, nb);
+      if (!(ok = warp_wait(bar(B_ACCFULL + a), (afph >> a) & 1u, wctx))) break;
+      afph ^= 1u << a;
+      tc_fence_after();
+      const int col0 = nb * BN + 2 * static_cast<int>(lane & 3);
+#pragma unroll 1
+      for (int hl = 0; hl < 2; ++hl) {
+        const int ra = mb * BM + static_cast<int>(quad * 32 + hl * 16 + (lane >> 2));   // rows ra and ra + 8
+        const bool la = ra < p.M, lb = ra + 8 < p.M;
+#pragma unroll 1
+        for (int ch = 0; ch < BN / 64; ++ch) {
+          uint32_t r[32];
+          tmem_ld16x256b_x8(tm + ((quad * 32u + hl * 16u) << 16) + a * BN + ch * 64, r);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int col = col0 + ch * 64 + 8 * k;
+            if (col >= p.N) continue;   // N is even, so col + 1 < N too
+            const float a0 = __uint_as_float(r[4 * k]), a1 = __uint_as_float(r[4 * k + 1]);
+            const float b0 = __uint_as_float(r[4 * k + 2]), b1 = __uint_as_float(r[4 * k + 3]);
+            if (p.c_fp32) {
+              float* c = static_cast<float*>(p.c);
+              if (la) *reinterpret_cast<float2*>(c + static_cast<size_t>(ra) * p.N + col) = make_float2(a0, a1);
+              if (lb) *reinterpret_cast<float2*>(c + static_cast<size_t>(ra + 8) * p.N + col) = make_float2(b0, b1);
+            } else {
+              uint16_t* c = static_cast<uint16_t*>(p.c);
+              if (la) *reinterpret_cast<uint32_t*>(c + static_cast<size_t>(ra) * p.N + col) = pack_bf16x2(a0, a1);
+              if (lb) *reinterpret_cast<uint32_t*>(c + static_cast<size_t>(ra + 8) * p.N + col) = pack_bf16x2(b0, b1);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_ACCEMPTY + a));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tm, 512);
+  }
+}
+
+}  // namespace
+
+int gemm_tile_rows() { return BM; }
+int gemm_tile_cols() { return BN; }
+int gemm_tile_depth() { return BK; }
+
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int num_sms,
+                        cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  const int grid = min(p.num_tiles, num_sms);
+  if (grid <= 0) return cudaSuccess;
+  gemm_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace gbattn

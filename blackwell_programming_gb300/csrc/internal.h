@@ -75,4 +75,20 @@ cudaError_t launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const De
 cudaError_t launch_combine(const DecodeParams& p, int grid, float* o, uint16_t* o_bf16, float* lse,
                            cudaStream_t stream);
 
+// Projection GEMM: C [M, N] = A [M, K] B [N, K]^T, bf16 in, fp32 accumulate,
+// bf16 or fp32 out; 128 x 256 output tiles walked by persistent CTAs.
+struct GemmParams {
+  void* c;             // bf16 or fp32 C [M, N]
+  int M, N, K;
+  int c_fp32;          // 1: C is fp32, 0: bf16
+  int tiles_m, tiles_n, num_tiles;
+  unsigned* err;
+};
+
+int gemm_tile_rows();
+int gemm_tile_cols();
+int gemm_tile_depth();
+cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int num_sms,
+                        cudaStream_t stream);
+
 }  // namespace gbattn

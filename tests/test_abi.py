@@ -1,4 +1,4 @@
-"""The C-ABI library builds, loads and exports what include/gbattn.h declares.
+"""The C-ABI library builds, loads and exports what include/*.h declare.
 
 These run without a GPU: only calls that return before touching CUDA are made
 (argument checks), no compute.
@@ -12,7 +12,8 @@ import pytest
 import blackwell_programming_gb300 as gb
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "gbattn.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if h.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -22,9 +23,12 @@ def lib():
 
 
 def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", src, flags=re.M)))
+    """Every function the headers in include/ declare."""
+    names = set()
+    for h in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:attn|gemm)_\w+)\s*\(", src, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_abi():
@@ -94,3 +98,19 @@ def test_unsupported_shapes(lib, bad):
 
 def test_v_longer_than_k_alias_rejected(lib):
     assert call(v_ptr=P * 2, d_qk=64, d_v=128) == gb.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bad", [
+    dict(a=0), dict(b=0), dict(c=0), dict(M=0), dict(N=-2), dict(K=0),
+    dict(K=12),          # rows of A and B must be whole 16-byte units
+    dict(N=7),           # C columns are stored in pairs
+    dict(a=P + 8), dict(b=P + 4), dict(c=P + 2),
+])
+def test_gemm_invalid_arguments(lib, bad):
+    a = dict(a=P, b=P * 2, c=P * 3, M=256, N=512, K=128)
+    a.update(bad)
+    assert gb.gemm_raw(a["a"], a["b"], a["c"], a["M"], a["N"], a["K"], False) == gb.ATTN_ERR_INVALID_ARG
+
+
+def test_gemm_sizes_past_32_bit_rows(lib):
+    assert gb.gemm_raw(P, P * 2, P * 3, 1 << 20, 4096, 4096, False) == gb.ATTN_ERR_UNSUPPORTED
