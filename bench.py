@@ -37,7 +37,8 @@ DEFAULT_WORKLOAD = "gqa_causal_d128"
 L2_FLUSH_BYTES = 256 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = {"prefill": "blackwell_programming_gb300/csrc/prefill_sm103.cu",
+KERNEL_SOURCES = {"gemm": "blackwell_programming_gb300/csrc/gemm_sm103.cu",
+                  "prefill": "blackwell_programming_gb300/csrc/prefill_sm103.cu",
                   "decode": "blackwell_programming_gb300/csrc/decode_sm103.cu",
                   "latent_prefill": "blackwell_programming_gb300/csrc/decode_sm103.cu"}
 
@@ -391,12 +392,160 @@ def run_ours(args, wl):
     return 0
 
 
+# ------------------------------------------------------- projection GEMM
+
+METRIC_GEMM = "projection GEMM TFLOP/s (bf16, 1 GB300) and % of dense BF16 tensor peak"
+_GEMM_SAMPLE = {}
+
+
+def gemm_oracle_sample(gw, budget_s: float):
+    """Time the fp64 GEMM oracle on whole rows of the workload, bounded in time."""
+    from oracle import gemm_nt
+    if gw.name not in _GEMM_SAMPLE:
+        # the first 256 rows of A and all of B, exactly as the GPU run draws them
+        rows = min(gw.M, 256)
+        a = syn.f32_to_bf16_bits(syn.normals_f32(gw.seed, 0, rows * gw.K)).reshape(rows, gw.K)
+        b = syn.f32_to_bf16_bits(syn.normals_f32(gw.seed, gw.M * gw.K, gw.N * gw.K)).reshape(gw.N, gw.K)
+        _GEMM_SAMPLE[gw.name] = (syn.bf16_bits_to_f64(a), syn.bf16_bits_to_f64(b))
+    a64, b64 = _GEMM_SAMPLE[gw.name]
+    rows, flops, t0 = 0, 0.0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and rows < a64.shape[0]:
+        blk = a64[rows:rows + 16]
+        gemm_nt(blk, b64)
+        rows += blk.shape[0]
+        flops += 2.0 * blk.shape[0] * gw.N * gw.K
+    secs = time.perf_counter() - t0
+    return flops / secs / 1e12, "%d of %d rows of %s (all %d columns), fp64 numpy" % (rows, gw.M, gw.name, gw.N), \
+        os.cpu_count() or 1
+
+
+def gemm_config(gw):
+    return {"workload": gw.name, "M": gw.M, "N": gw.N, "K": gw.K, "a": "bf16 [M, K]", "b": "bf16 [N, K]",
+            "c": "bf16 [M, N]", "inputs": "seeded N(0,1) bf16",
+            "l2": "flushed (256 MB write) before every step, outside the step events", "parallelism": "replicas"}
+
+
+def run_gemm_reference(args, gw):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    t0 = time.time()
+    vals, desc, cores = [], "", 1
+    for _ in range(args.warmup):
+        gemm_oracle_sample(gw, 0.5)
+    for _ in range(args.steps):
+        v, desc, cores = gemm_oracle_sample(gw, args.ref_budget)
+        vals.append(v)
+    value = statistics.median(vals)
+    print(json.dumps({"impl": "reference", "metric": METRIC_GEMM, "value": value, "unit": "TFLOP/s",
+                      "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": gemm_config(gw),
+                      "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                       "sample": desc},
+                      "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                      "wall_s": round(time.time() - t0, 1)}), flush=True)
+    return 0
+
+
+def run_gemm_ours(args, gw):
+    import numpy as np
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    import blackwell_programming_gb300 as gb
+    gb.build()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, cores = gemm_oracle_sample(gw, args.ref_budget)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    a_bits, b_bits = syn.make_gemm_inputs(gw)
+    ha = torch.from_numpy(a_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hb = torch.from_numpy(b_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    a, b = ha.cuda(), hb.cuda()
+    c = torch.empty((gw.M, gw.N), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    clocks = ClockSampler(int(vis[local]) if local < len(vis) and vis[local].strip().isdigit() else local)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            gb.gemm_nt(a, b, out=c, stream=stream)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        for s_ev, e_ev in ev:
+            flush.fill_(1.0)
+            s_ev.record(stream)
+            gb.gemm_nt(a, b, out=c, stream=stream)
+            e_ev.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    assert gb.attn_check_device(stream) == 0, "kernel reported a timed-out wait"
+    clk = clocks.stop()
+    times = [s_ev.elapsed_time(e_ev) / 1e3 for s_ev, e_ev in ev]
+    total = sum(times)
+    t_max = reduce_max(total, world)
+    value = aggregate(gw.flops * args.steps, t_max, world) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        hc = torch.empty((gw.M, gw.N), dtype=torch.bfloat16).pin_memory()
+        da, db = torch.empty_like(a), torch.empty_like(b)
+        with torch.cuda.stream(stream):
+            def step():
+                da.copy_(ha, non_blocking=True)
+                db.copy_(hb, non_blocking=True)
+                gb.gemm_nt(da, db, out=c, stream=stream)
+                hc.copy_(c, non_blocking=True)
+            for _ in range(args.warmup):
+                step()
+            torch.cuda.synchronize()
+            s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_ev.record(stream)
+            for _ in range(args.steps):
+                step()
+            e_ev.record(stream)
+            torch.cuda.synchronize()
+        e2e_max = reduce_max(s_ev.elapsed_time(e_ev) / 1e3, world)
+        e2e = {"value": aggregate(gw.flops * args.steps, e2e_max, world) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 2 * (gw.M + gw.N) * gw.K, "d2h_bytes_per_step": 2 * gw.M * gw.N}
+
+    peaks, peak_src = load_peaks()
+    per_launch = total / args.steps
+    achieved = gw.flops / per_launch / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"], "peak_source": peak_src + " bf16_tflops (burst)",
+            "kernel": "gemm_kernel", "algorithmic_flops_per_launch": gw.flops,
+            "traffic": committed_traffic("gemm", gw.name)}
+    if rank == 0:
+        print(json.dumps({"metric": METRIC_GEMM, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                          "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                          "config": gemm_config(gw), "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                          "gpu_launches": args.steps, "clocks": clk,
+                          "step_ms": {"min": min(times) * 1e3, "median": statistics.median(times) * 1e3,
+                                      "max": max(times) * 1e3}}), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(syn.WORKLOADS) + sorted(syn.GEMM_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -408,6 +557,9 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)      # at least three untimed warm-up steps
     global O_DTYPE
     O_DTYPE = args.out
+    if args.workload in syn.GEMM_WORKLOADS:
+        gw = syn.GEMM_WORKLOADS[args.workload]
+        return run_gemm_reference(args, gw) if args.impl == "reference" else run_gemm_ours(args, gw)
     wl = syn.WORKLOADS[args.workload]
     if args.batch is not None:
         wl = wl.with_sizes(B=args.batch, name="%s_B%d" % (wl.name, args.batch))

@@ -194,3 +194,36 @@ def make_inputs(wl: Workload) -> Inputs:
     k = _draw(wl.seed, nq, ks, wl.kv_factor)
     v = None if wl.v_aliases_k else _draw(wl.seed, nq + nk, vs, wl.kv_factor)
     return Inputs(q, k, v, wl)
+
+
+@dataclass(frozen=True)
+class GemmWorkload:
+    """One projection GEMM C [M, N] = A [M, K] B [N, K]^T (bf16 in, bf16 out)."""
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int = 0
+
+    @property
+    def flops(self) -> float:
+        return 2.0 * self.M * self.N * self.K
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """A and B read once, C (bf16) written once."""
+        return 2 * (self.M * self.K + self.N * self.K + self.M * self.N)
+
+
+GEMM_WORKLOADS = {
+    # the QKV projection in front of gqa_causal_d128: 4 x 4096 tokens of a
+    # 4096-wide model into 32 query + 8 key + 8 value heads of 128
+    "gemm_qkv_proj": GemmWorkload("gemm_qkv_proj", 16384, 6144, 4096),
+}
+
+
+def make_gemm_inputs(gw: GemmWorkload):
+    """bf16 bit patterns of A [M, K] and B [N, K] from the workload's seed, A first."""
+    a = f32_to_bf16_bits(normals_f32(gw.seed, 0, gw.M * gw.K)).reshape(gw.M, gw.K)
+    b = f32_to_bf16_bits(normals_f32(gw.seed, gw.M * gw.K, gw.N * gw.K)).reshape(gw.N, gw.K)
+    return a, b
