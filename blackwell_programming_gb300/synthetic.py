@@ -227,3 +227,73 @@ def make_gemm_inputs(gw: GemmWorkload):
     a = f32_to_bf16_bits(normals_f32(gw.seed, 0, gw.M * gw.K)).reshape(gw.M, gw.K)
     b = f32_to_bf16_bits(normals_f32(gw.seed, gw.M * gw.K, gw.N * gw.K)).reshape(gw.N, gw.K)
     return a, b
+
+
+@dataclass(frozen=True)
+class LayerWorkload:
+    """One attention layer slice Y = Attn(X W_qkv^T) W_o^T over B sequences of N tokens.
+
+    X ~ N(0, 1); both weights ~ N(0, 1) / sqrt(fan-in) (scaled in fp32 before
+    the bf16 rounding), so Q, K, V and Y come out with unit variance, as in
+    the attention workloads.
+    """
+    name: str
+    B: int
+    N: int
+    d_model: int
+    Hq: int
+    Hkv: int
+    d: int
+    causal: bool
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def n_qkv(self) -> int:
+        return (self.Hq + 2 * self.Hkv) * self.d
+
+    @property
+    def flops(self) -> float:
+        """QKV GEMM + attention (halved when causal, as for the attention lines) + O GEMM."""
+        t = self.B * self.N
+        att = 4.0 * self.B * self.Hq * self.N * self.N * self.d
+        if self.causal:
+            att /= 2.0
+        return 2.0 * t * self.n_qkv * self.d_model + att + 2.0 * t * self.d_model * self.Hq * self.d
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """X, W_qkv, W_o read; QKV and O written and read back once; Y (bf16) written."""
+        t = self.B * self.N
+        x = t * self.d_model
+        w = self.n_qkv * self.d_model + self.d_model * self.Hq * self.d
+        qkv = t * self.n_qkv
+        o = t * self.Hq * self.d
+        return 2 * (x + w + 2 * qkv + 2 * o + t * self.d_model)
+
+    def with_sizes(self, **kw) -> "LayerWorkload":
+        d = dict(self.__dict__)
+        d.update(kw)
+        return LayerWorkload(**d)
+
+
+LAYER_WORKLOADS = {
+    # the layer around gqa_causal_d128: a 4096-wide model, 32 query and 8 KV
+    # heads of 128, 4 sequences of 4096 tokens
+    "layer_gqa_d128": LayerWorkload("layer_gqa_d128", 4, 4096, 4096, 32, 8, 128, True),
+}
+
+
+def make_layer_inputs(lw: LayerWorkload):
+    """bf16 bit patterns of X [B*N, d_model], W_qkv [(Hq+2Hkv)*d, d_model] and
+    W_o [d_model, Hq*d], drawn in that order from the workload's seed."""
+    t = lw.B * lw.N
+    nx = t * lw.d_model
+    nw = lw.n_qkv * lw.d_model
+    x = _draw(lw.seed, 0, (t, lw.d_model), 1.0)
+    w_qkv = _draw(lw.seed, nx, (lw.n_qkv, lw.d_model), 1.0 / math.sqrt(lw.d_model))
+    w_o = _draw(lw.seed, nx + nw, (lw.d_model, lw.Hq * lw.d), 1.0 / math.sqrt(lw.Hq * lw.d))
+    return x, w_qkv, w_o
