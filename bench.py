@@ -540,12 +540,217 @@ def run_gemm_ours(args, gw):
     return 0
 
 
+# ------------------------------------------------------ attention layer slice
+
+METRIC_LAYER = "attention layer slice TFLOP/s (QKV GEMM + attention + O GEMM, bf16, 1 GB300)"
+_LAYER_SAMPLE = {}
+
+
+def layer_oracle_sample(lw, budget_s: float):
+    """Time the fp64 layer oracle on sequence 0 of the workload: its K and V
+    projections, then blocks of 32 query tokens (Q projection, attention
+    rows of every head, O projection) until the budget is spent.  FLOPs are
+    credited as the GPU line counts them (per token, the causal attention's
+    halved average)."""
+    import numpy as np
+    from oracle import attention_head, gemm_nt, kv_head_of, round_bf16
+    if lw.name not in _LAYER_SAMPLE:
+        N, D = lw.N, lw.d_model
+        x = syn.f32_to_bf16_bits(syn.normals_f32(lw.seed, 0, N * D)).reshape(N, D)
+        x_all = lw.B * lw.N * D
+        nw = lw.n_qkv * D
+        wq = syn._draw(lw.seed, x_all, (lw.n_qkv, D), 1.0 / (D ** 0.5))
+        wo = syn._draw(lw.seed, x_all + nw, (D, lw.Hq * lw.d), 1.0 / ((lw.Hq * lw.d) ** 0.5))
+        _LAYER_SAMPLE[lw.name] = tuple(syn.bf16_bits_to_f64(t) for t in (x, wq, wo))
+    x, wq, wo = _LAYER_SAMPLE[lw.name]
+    Hq, Hkv, d, N = lw.Hq, lw.Hkv, lw.d, lw.N
+    t0 = time.perf_counter()
+    kv = round_bf16(gemm_nt(x, wq[Hq * d:]))
+    flops = 2.0 * N * 2 * Hkv * d * lw.d_model
+    per_tok = 2.0 * Hq * d * lw.d_model * 2 + 4.0 * Hq * d * N / (2.0 if lw.causal else 1.0)
+    done = 0
+    while time.perf_counter() - t0 < budget_s and done < N:
+        toks = list(range(done, min(N, done + 32)))
+        q = round_bf16(gemm_nt(x[toks], wq[:Hq * d]))
+        o = np.zeros((len(toks), Hq * d))
+        for h in range(Hq):
+            g = kv_head_of(h, Hq, Hkv)
+            o[:, h * d:(h + 1) * d], _ = attention_head(q[:, h * d:(h + 1) * d], kv[:, g * d:(g + 1) * d],
+                                                        kv[:, (Hkv + g) * d:(Hkv + g + 1) * d], lw.causal,
+                                                        lw.scale, row_index=toks, n_q=N)
+        gemm_nt(round_bf16(o), wo)
+        done += len(toks)
+        flops += per_tok * len(toks)
+    secs = time.perf_counter() - t0
+    return flops / secs / 1e12, ("sequence 0 of %s: K/V projections of all %d tokens, then %d query tokens "
+                                 "through Q projection, attention and O projection, fp64 numpy") % (
+        lw.name, N, done), os.cpu_count() or 1
+
+
+def layer_config(lw):
+    return {"workload": lw.name, "B": lw.B, "N": lw.N, "d_model": lw.d_model, "Hq": lw.Hq, "Hkv": lw.Hkv,
+            "d": lw.d, "causal": lw.causal, "scale": lw.scale,
+            "x": "bf16 [B*N, d_model]", "w_qkv": "bf16 [(Hq+2Hkv)*d, d_model]", "w_o": "bf16 [d_model, Hq*d]",
+            "qkv": "bf16 token-major, read in place by the attention", "o": "bf16 token-major", "y": "bf16",
+            "inputs": "seeded N(0,1) X, N(0,1)/sqrt(fan-in) weights, bf16",
+            "l2": "flushed (256 MB write) before every step, outside the step events", "parallelism": "replicas"}
+
+
+def run_layer_reference(args, lw):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    t0 = time.time()
+    vals, desc, cores = [], "", 1
+    for _ in range(args.warmup):
+        layer_oracle_sample(lw, 0.5)
+    for _ in range(args.steps):
+        v, desc, cores = layer_oracle_sample(lw, args.ref_budget)
+        vals.append(v)
+    value = statistics.median(vals)
+    print(json.dumps({"impl": "reference", "metric": METRIC_LAYER, "value": value, "unit": "TFLOP/s",
+                      "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": layer_config(lw),
+                      "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                       "sample": desc},
+                      "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                      "wall_s": round(time.time() - t0, 1)}), flush=True)
+    return 0
+
+
+def run_layer_ours(args, lw):
+    import numpy as np
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    import blackwell_programming_gb300 as gb
+    gb.build()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, cores = layer_oracle_sample(lw, args.ref_budget)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    B, N, D, Hq, Hkv, d = lw.B, lw.N, lw.d_model, lw.Hq, lw.Hkv, lw.d
+    T, nqkv, nq = B * N, lw.n_qkv, lw.Hq * lw.d
+    x_bits, wq_bits, wo_bits = syn.make_layer_inputs(lw)
+    pin = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hx, hwq, hwo = pin(x_bits), pin(wq_bits), pin(wo_bits)
+    x, wq, wo = hx.cuda(), hwq.cuda(), hwo.cuda()
+    qkv = torch.empty((T, nqkv), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty((T, nq), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((T, D), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+    L = gb.load_library()
+    import ctypes
+    P = lambda t, off=0: ctypes.c_void_p(t.data_ptr() + 2 * off)
+
+    def qkv_gemm():
+        return L.gemm_bf16_nt(P(x), P(wq), P(qkv), T, nqkv, D, 0, ctypes.c_void_p(sp))
+
+    def attention():
+        return L.attn_fwd_bshd(P(qkv), P(qkv, nq), P(qkv, nq + Hkv * d), P(o), None, B, Hq, Hkv, N, N, d,
+                               nqkv, nqkv, nqkv, nq, 0, 1 if lw.causal else 0, ctypes.c_float(lw.scale),
+                               ctypes.c_void_p(sp))
+
+    def o_gemm():
+        return L.gemm_bf16_nt(P(o), P(wo), P(y), T, D, nq, 0, ctypes.c_void_p(sp))
+
+    parts = (("qkv_gemm", qkv_gemm), ("attention", attention), ("o_gemm", o_gemm))
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    clocks = ClockSampler(int(vis[local]) if local < len(vis) and vis[local].strip().isdigit() else local)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.fill_(1.0)
+            for _, fn in parts:
+                assert fn() == 0
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        for e in ev:
+            flush.fill_(1.0)
+            e[0].record(stream)
+            for i, (_, fn) in enumerate(parts):
+                fn()
+                e[i + 1].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    assert gb.attn_check_device(stream) == 0, "kernel reported a timed-out wait"
+    clk = clocks.stop()
+    part_s = [[e[i].elapsed_time(e[i + 1]) / 1e3 for i in range(3)] for e in ev]
+    times = [sum(p) for p in part_s]
+    total = sum(times)
+    t_max = reduce_max(total, world)
+    value = aggregate(lw.flops * args.steps, t_max, world) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        hy = torch.empty((T, D), dtype=torch.bfloat16).pin_memory()
+        dx = torch.empty_like(x)
+        with torch.cuda.stream(stream):
+            def step():
+                dx.copy_(hx, non_blocking=True)
+                st = gb.attn_layer_raw(dx.data_ptr(), wq.data_ptr(), wo.data_ptr(), qkv.data_ptr(), o.data_ptr(),
+                                       y.data_ptr(), 0, B, N, D, Hq, Hkv, d, lw.causal, lw.scale, False, sp)
+                assert st == 0
+                hy.copy_(y, non_blocking=True)
+            for _ in range(args.warmup):
+                step()
+            torch.cuda.synchronize()
+            s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_ev.record(stream)
+            for _ in range(args.steps):
+                step()
+            e_ev.record(stream)
+            torch.cuda.synchronize()
+        e2e_max = reduce_max(s_ev.elapsed_time(e_ev) / 1e3, world)
+        e2e = {"value": aggregate(lw.flops * args.steps, e2e_max, world) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": 2 * T * D, "d2h_bytes_per_step": 2 * T * D,
+               "api": "attn_layer_fwd (one call), weights resident"}
+
+    # per-part FLOPs in the line's convention; the roofline is the slowest part's kernel
+    att = 4.0 * B * Hq * N * N * d / (2.0 if lw.causal else 1.0)
+    pflops = {"qkv_gemm": 2.0 * T * nqkv * D, "attention": att, "o_gemm": 2.0 * T * D * nq}
+    mean_s = {name: sum(p[i] for p in part_s) / args.steps for i, (name, _) in enumerate(parts)}
+    top = max(mean_s, key=mean_s.get)
+    peaks, peak_src = load_peaks()
+    achieved = pflops[top] / mean_s[top] / 1e12
+    kern = {"qkv_gemm": ("gemm_kernel", "gemm", "gemm_qkv_proj"), "attention": ("prefill_kernel", "prefill", None),
+            "o_gemm": ("gemm_kernel", "gemm", None)}[top]
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"], "peak_source": peak_src + " bf16_tflops (burst)",
+            "kernel": kern[0] + " (" + top + ")", "algorithmic_flops_per_launch": pflops[top],
+            "traffic": committed_traffic(kern[1], kern[2]) if kern[2] else None}
+    if rank == 0:
+        print(json.dumps({"metric": METRIC_LAYER, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                          "data": "synthetic", "config": layer_config(lw), "roofline": roof, "cpu_baseline": cpu,
+                          "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clk,
+                          "parts": {name: {"ms": mean_s[name] * 1e3,
+                                           "tflops": pflops[name] / mean_s[name] / 1e12} for name, _ in parts},
+                          "step_ms": {"min": min(times) * 1e3, "median": statistics.median(times) * 1e3,
+                                      "max": max(times) * 1e3}}), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(syn.WORKLOADS) + sorted(syn.GEMM_WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(syn.WORKLOADS) + sorted(syn.GEMM_WORKLOADS) + sorted(syn.LAYER_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -560,6 +765,11 @@ def main(argv=None):
     if args.workload in syn.GEMM_WORKLOADS:
         gw = syn.GEMM_WORKLOADS[args.workload]
         return run_gemm_reference(args, gw) if args.impl == "reference" else run_gemm_ours(args, gw)
+    if args.workload in syn.LAYER_WORKLOADS:
+        lw = syn.LAYER_WORKLOADS[args.workload]
+        if args.batch is not None:
+            lw = lw.with_sizes(B=args.batch, name="%s_B%d" % (lw.name, args.batch))
+        return run_layer_reference(args, lw) if args.impl == "reference" else run_layer_ours(args, lw)
     wl = syn.WORKLOADS[args.workload]
     if args.batch is not None:
         wl = wl.with_sizes(B=args.batch, name="%s_B%d" % (wl.name, args.batch))

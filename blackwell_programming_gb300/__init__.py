@@ -2,7 +2,8 @@
 
 The compute path is libgbattn.so (hand-written CUDA with tcgen05, TMA and
 mbarrier inline PTX) behind the C ABI of include/gbattn.h (attention) and
-include/gbgemm.h (the projection GEMM around it); this package is a thin
+include/gbgemm.h and include/gblayer.h (the projection GEMMs around it and
+the layer slice they form); this package is a thin
 ctypes binding over it plus the seeded synthetic-input generator.
 """
 from . import _build
@@ -11,7 +12,8 @@ from .binding import (ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG, ATTN_ERR_NO_DEVICE, A
                       attn_check_device, attn_decode_fwd_noalloc,
                       attn_decode_workspace_bytes, attn_fwd, attn_fwd_raw, attn_last_cuda_error,
                       attn_status_string,
-                      attn_version, gemm_nt, gemm_raw, load_library)
+                      attn_version, attn_fwd_bshd, attn_layer_fwd, attn_layer_raw, gemm_nt, gemm_raw,
+                      load_library)
 
 
 def build(force: bool = False) -> str:
@@ -25,4 +27,4 @@ __all__ = ["build", "attn_fwd", "attn_fwd_raw", "attn_check_device", "attn_statu
            "attn_version", "attn_decode_workspace_bytes", "attn_last_cuda_error", "AttnError", "load_library", "EXPORTS",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
            "ATTN_ERR_TIMEOUT", "ATTN_ERR_NO_DEVICE", "ATTN_ERR_SCRATCH_LIMIT", "attn_decode_fwd_noalloc",
-           "gemm_nt", "gemm_raw"]
+           "gemm_nt", "gemm_raw", "attn_fwd_bshd", "attn_layer_fwd", "attn_layer_raw"]

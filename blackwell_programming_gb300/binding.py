@@ -23,7 +23,8 @@ ATTN_ERR_SCRATCH_LIMIT = 6
 
 # Symbols the shared library exports (the declarations of include/gbattn.h).
 EXPORTS = ("attn_fwd", "attn_fwd_bf16out", "attn_check_device", "attn_status_string", "attn_last_cuda_error",
-           "attn_version", "attn_decode_workspace_bytes", "attn_decode_fwd_noalloc", "gemm_bf16_nt")
+           "attn_version", "attn_decode_workspace_bytes", "attn_decode_fwd_noalloc", "gemm_bf16_nt",
+           "attn_fwd_bshd", "attn_layer_fwd")
 
 _lib = None
 
@@ -49,6 +50,11 @@ def load_library(path: str | None = None):
     L.attn_fwd.restype = i
     L.attn_fwd_bf16out.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, vp]
     L.attn_fwd_bf16out.restype = i
+    ll = ctypes.c_longlong
+    L.attn_fwd_bshd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, ll, ll, ll, ll, i, i, f, vp]
+    L.attn_fwd_bshd.restype = i
+    L.attn_layer_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+    L.attn_layer_fwd.restype = i
     L.gemm_bf16_nt.argtypes = [vp, vp, vp, i, i, i, i, vp]
     L.gemm_bf16_nt.restype = i
     L.attn_check_device.argtypes = [vp, i]
@@ -235,3 +241,131 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None
     if st != ATTN_OK:
         _raise(L, st, fn.__name__)
     return out, lse
+
+
+def _token_major_ld(name, t, heads, d):
+    """Token stride (elements) of a [B, N, H, d] tensor whose heads sit side by
+    side in each token's row, as attn_fwd_bshd reads it."""
+    B, N, H, dd = t.shape
+    if H != heads or dd != d:
+        raise ValueError("%s must be [B, N, %d, %d], got %s" % (name, heads, d, tuple(t.shape)))
+    sb, sn, sh, sc = t.stride()
+    if sc != 1 or sh != d or sn % 8 != 0 or sn < heads * d or (B > 1 and sb != N * sn):
+        raise ValueError("%s must be token-major: strides (N*ld, ld, d, 1) with ld %% 8 == 0 and "
+                         "ld >= H*d, got %s" % (name, t.stride()))
+    if t.data_ptr() % 16 != 0:
+        raise ValueError("%s must start on a 16-byte boundary" % name)
+    return sn
+
+
+def attn_fwd_bshd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                  want_lse: bool = True, stream=None, out_dtype=None):
+    """Attention on token-major tensors (attn_fwd_bshd in gbattn.h).
+
+    q: bf16 [B, Nq, Hq, d], k and v: bf16 [B, Nkv, Hkv, d], d 64 or 128, each
+    with strides (N * ld, ld, d, 1): for example column slices of a QKV
+    projection's output viewed as [B, N, H, d].  Returns (o [B, Nq, Hq, d],
+    lse fp32 [B, Hq, Nq] or None); O is bf16 unless ``out_dtype`` (or
+    ``out``) says fp32.
+    """
+    import torch
+    L = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4:
+            raise TypeError("%s must be a 4-D bfloat16 CUDA tensor [B, N, H, d]" % name)
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
+    B, Nq, Hq, d = q.shape
+    Bk, Nkv, Hkv, _ = k.shape
+    if Bk != B or v.shape[0] != B or v.shape[1] != Nkv:
+        raise ValueError("shape mismatch: q %s k %s v %s" % (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
+    q_ld = _token_major_ld("q", q, Hq, d)
+    k_ld = _token_major_ld("k", k, Hkv, d)
+    v_ld = _token_major_ld("v", v, Hkv, d)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = q.device
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.bfloat16
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("O is fp32 or bf16, not %s" % out_dtype)
+    if out is None:
+        out = torch.empty((B, Nq, Hq, d), dtype=out_dtype, device=dev)
+    elif out.dtype != out_dtype or out.device != dev or out.dim() != 4 or out.shape[:2] != (B, Nq):
+        raise ValueError("out must be a %s [B, Nq, Hq, d] tensor on q's device" % out_dtype)
+    o_ld = _token_major_ld("out", out, Hq, d)
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    elif lse is not None and (lse.shape != (B, Hq, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [B, Hq, Nq] tensor")
+    with torch.cuda.device(dev):
+        st = L.attn_fwd_bshd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                             ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                             ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
+                             B, Hq, Hkv, Nq, Nkv, d, q_ld, k_ld, v_ld, o_ld,
+                             1 if out_dtype == torch.float32 else 0, 1 if causal else 0, ctypes.c_float(scale),
+                             _stream_handle(stream, dev))
+    if st != ATTN_OK:
+        _raise(L, st, "attn_fwd_bshd")
+    return out, lse
+
+
+def attn_layer_raw(x_ptr: int, w_qkv_ptr: int, w_o_ptr: int, qkv_ptr: int, o_ptr: int, y_ptr: int, lse_ptr: int,
+                   B: int, N: int, d_model: int, Hq: int, Hkv: int, d: int, causal: bool, scale: float,
+                   y_fp32: bool, stream_ptr: int = 0) -> int:
+    """The C call attn_layer_fwd with raw integer pointers; returns the status code."""
+    L = load_library()
+    return L.attn_layer_fwd(*(ctypes.c_void_p(p) for p in (x_ptr, w_qkv_ptr, w_o_ptr, qkv_ptr, o_ptr, y_ptr,
+                                                          lse_ptr)),
+                            B, N, d_model, Hq, Hkv, d, 1 if causal else 0, ctypes.c_float(scale),
+                            1 if y_fp32 else 0, ctypes.c_void_p(stream_ptr))
+
+
+def attn_layer_fwd(x, w_qkv, w_o, Hq: int, Hkv: int, causal: bool = True, scale: float | None = None,
+                   y_dtype=None, want_lse: bool = False, qkv=None, o=None, y=None, stream=None):
+    """Y = Attn(X W_qkv^T) W_o^T (attn_layer_fwd in gblayer.h).
+
+    x: bf16 [B, N, d_model]; w_qkv: bf16 [(Hq + 2 Hkv) d, d_model] (W_q rows,
+    then W_k, then W_v); w_o: bf16 [d_model, Hq d].  Returns (y [B, N,
+    d_model], qkv bf16 [B, N, (Hq + 2 Hkv) d], o bf16 [B, N, Hq d], lse fp32
+    [B, Hq, N] or None); y is bf16 unless ``y_dtype`` is torch.float32.
+    """
+    import torch
+    L = load_library()
+    for name, t, nd in (("x", x, 3), ("w_qkv", w_qkv, 2), ("w_o", w_o, 2)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != nd:
+            raise TypeError("%s must be a %d-D bfloat16 CUDA tensor" % (name, nd))
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    B, N, d_model = x.shape
+    rows, kq = w_qkv.shape
+    if kq != d_model or rows % (Hq + 2 * Hkv) != 0:
+        raise ValueError("w_qkv must be [(Hq + 2 Hkv) d, d_model], got %s" % (tuple(w_qkv.shape),))
+    d = rows // (Hq + 2 * Hkv)
+    if tuple(w_o.shape) != (d_model, Hq * d):
+        raise ValueError("w_o must be [d_model, Hq d] = %s, got %s" % ((d_model, Hq * d), tuple(w_o.shape)))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if y_dtype is None:
+        y_dtype = y.dtype if y is not None else torch.bfloat16
+    dev = x.device
+
+    def buf(t, shape, dtype, name):
+        if t is None:
+            return torch.empty(shape, dtype=dtype, device=dev)
+        if tuple(t.shape) != shape or t.dtype != dtype or not t.is_contiguous() or t.device != dev:
+            raise ValueError("%s must be a contiguous %s %s tensor on x's device" % (name, dtype, shape))
+        return t
+
+    qkv = buf(qkv, (B, N, rows), torch.bfloat16, "qkv")
+    o = buf(o, (B, N, Hq * d), torch.bfloat16, "o")
+    y = buf(y, (B, N, d_model), y_dtype, "y")
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev) if want_lse else None
+    with torch.cuda.device(dev):
+        st = L.attn_layer_fwd(*(ctypes.c_void_p(t.data_ptr()) for t in (x, w_qkv, w_o, qkv, o, y)),
+                              ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
+                              B, N, d_model, Hq, Hkv, d, 1 if causal else 0, ctypes.c_float(scale),
+                              1 if y_dtype == torch.float32 else 0, _stream_handle(stream, dev))
+    if st != ATTN_OK:
+        _raise(L, st, "attn_layer_fwd")
+    return y, qkv, o, lse

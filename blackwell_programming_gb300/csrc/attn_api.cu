@@ -7,7 +7,10 @@
 // engine's descriptor is derived, with the swizzle chosen from the tile
 // width): every [B, H, N, d] tensor is described as a 3-D box grid
 // (d, N, B*H) with 64-feature (128-byte) boxes and the 128-byte swizzle, so a
-// tile that runs past N reads zeros instead of the next head's rows.
+// tile that runs past N reads zeros instead of the next head's rows.  The
+// prefill kernel takes 4-D maps (d, N, H, B), or (d, H, N, B) for the
+// token-major [B, N, H, d] layout that a projection GEMM writes, so Q, K and V
+// can be read where the QKV GEMM left them.
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -19,6 +22,7 @@
 
 #include "gbattn.h"
 #include "gbgemm.h"
+#include "gblayer.h"
 #include "internal.h"
 
 namespace gbattn {
@@ -121,6 +125,44 @@ int make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, ui
   return ATTN_OK;
 }
 
+// 4-D bf16 tensor map with a 64 x box1 x box2 x 1 box and the 128-byte
+// swizzle.  Strides are in bytes, for dimensions 1..3.
+int make_map4(CUtensorMap* m, const void* base, const uint64_t dims[4], const uint64_t strides[3], uint32_t box1,
+              uint32_t box2) {
+  cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t gs[3] = {strides[0], strides[1], strides[2]};
+  cuuint32_t box[4] = {64u, box1, box2, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), gd, gs, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(t_cuda_error, sizeof(t_cuda_error), "cuTensorMapEncodeTiled (4-D) failed (CUresult %d)",
+                  static_cast<int>(r));
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+// Map of one prefill operand with H heads of N rows of d features per batch.
+// Head-major [B, H, N, d] (ld == 0): dimensions (d, N, H, B), 128-row boxes
+// along N.  Token-major (ld > 0 = elements from one token's row to the
+// next): element (b, h, i, c) at base + (b * N + i) * ld + h * d + c,
+// dimensions (d, H, N, B) so that the strides still grow with the dimension.
+int make_prefill_map(CUtensorMap* m, const void* base, int B, int H, int N, int d, long long ld) {
+  const uint64_t es = 2;
+  if (ld == 0) {
+    const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(N), static_cast<uint64_t>(H),
+                              static_cast<uint64_t>(B)};
+    const uint64_t st[3] = {es * d, es * d * N, es * d * N * H};
+    return make_map4(m, base, dims, st, 128, 1);
+  }
+  const uint64_t dims[4] = {static_cast<uint64_t>(d), static_cast<uint64_t>(H), static_cast<uint64_t>(N),
+                            static_cast<uint64_t>(B)};
+  const uint64_t st[3] = {es * d, es * static_cast<uint64_t>(ld), es * static_cast<uint64_t>(ld) * N};
+  return make_map4(m, base, dims, st, 1, 128);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool check_env() {
@@ -194,6 +236,53 @@ int attn_check_device(attn_stream_t stream, int reset) {
 
 namespace {
 
+// Token strides (elements) of Q, K, V and O; all zero = head-major
+// [B, H, N, d] for every operand.
+struct PrefillLayout {
+  long long q_ld, k_ld, v_ld, o_ld;
+};
+
+// The prefill kernel (d 64 or 128, d_v == d) on checked arguments.
+int run_prefill(const void* q, const void* k, const void* v, float* o32, uint16_t* o16, float* lse, int B, int Hq,
+                int Hkv, int Nq, int Nkv, int d, int causal, float scale_log2, const PrefillLayout& lay,
+                DeviceInfo* dev, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv;
+  int st;
+  if ((st = make_prefill_map(&tq, q, B, Hq, Nq, d, lay.q_ld)) != ATTN_OK) return st;
+  if ((st = make_prefill_map(&tk, k, B, Hkv, Nkv, d, lay.k_ld)) != ATTN_OK) return st;
+  if ((st = make_prefill_map(&tv, v, B, Hkv, Nkv, d, lay.v_ld)) != ATTN_OK) return st;
+  PrefillParams p{};
+  p.o = o32;
+  p.o_bf16 = o16;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Nq = Nq;
+  p.Nkv = Nkv;
+  p.d_v = d;
+  p.token_major = lay.q_ld != 0 ? 1 : 0;
+  if (lay.o_ld == 0) {
+    p.o_sr = d;
+    p.o_sh = static_cast<long long>(Nq) * d;
+    p.o_sb = p.o_sh * Hq;
+  } else {
+    p.o_sr = lay.o_ld;
+    p.o_sh = d;
+    p.o_sb = lay.o_ld * Nq;
+  }
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale_log2;
+  p.nqb = (Nq + 255) / 256;
+  p.nkv_tiles = (Nkv + 127) / 128;
+  p.num_units = B * Hq * p.nqb;
+  p.err = dev->err;
+  cudaError_t e;
+  if ((e = launch_prefill(d, tq, tk, tv, p, dev->num_sms, stream)) != cudaSuccess)
+    return cuda_fail(e, "prefill launch");
+  return ATTN_OK;
+}
+
 // attn_fwd and attn_fwd_bf16out: O is written as fp32 (o32) or bf16 (o16).
 int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint16_t* o16, float* lse, int B, int Hq,
                   int Hkv, int Nq, int Nkv, int d_qk, int d_v, int causal, float scale, attn_stream_t stream_) {
@@ -229,30 +318,10 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint1
   cudaError_t e;
 
   if (prefill) {
-    const int d = d_qk;
-    CUtensorMap tq, tk, tv;
-    const uint64_t rs = static_cast<uint64_t>(d) * 2;
-    if ((st = make_map(&tq, q, d, Nq, static_cast<uint64_t>(B) * Hq, rs, rs * Nq, 128)) != ATTN_OK) return st;
-    if ((st = make_map(&tk, k, d, Nkv, static_cast<uint64_t>(B) * Hkv, rs, rs * Nkv, 128)) != ATTN_OK) return st;
-    if ((st = make_map(&tv, v, d, Nkv, static_cast<uint64_t>(B) * Hkv, rs, rs * Nkv, 128)) != ATTN_OK) return st;
-    PrefillParams p{};
-    p.o = o32;
-    p.o_bf16 = o16;
-    p.lse = lse;
-    p.B = B;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.Nq = Nq;
-    p.Nkv = Nkv;
-    p.d_v = d_v;
-    p.causal = causal ? 1 : 0;
-    p.scale_log2 = scale_log2;
-    p.nqb = (Nq + 255) / 256;
-    p.nkv_tiles = (Nkv + 127) / 128;
-    p.num_units = B * Hq * p.nqb;
-    p.err = dev->err;
-    if ((e = launch_prefill(d, tq, tk, tv, p, dev->num_sms, stream)) != cudaSuccess)
-      return cuda_fail(e, "prefill launch");
+    const PrefillLayout lay{0, 0, 0, 0};
+    if ((st = run_prefill(q, k, v, o32, o16, lse, B, Hq, Hkv, Nq, Nkv, d_qk, causal, scale_log2, lay, dev,
+                          stream)) != ATTN_OK)
+      return st;
   } else if (!decode) {
     // latent shape, Nq > 1: the decode kernel in prefill mode
     CUtensorMap tq, tk;
@@ -363,6 +432,68 @@ int attn_fwd_bf16out(const void* q, const void* k, const void* v, void* o, float
   if (o == nullptr) return ATTN_ERR_INVALID_ARG;
   return attn_fwd_impl(q, k, v, nullptr, static_cast<uint16_t*>(o), lse, B, Hq, Hkv, Nq, Nkv, d_qk, d_v, causal,
                        scale, stream);
+}
+
+int attn_fwd_bshd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                  int Nkv, int d, long long q_ld, long long k_ld, long long v_ld, long long o_ld, int o_fp32,
+                  int causal, float scale, attn_stream_t stream_) {
+  t_cuda_error[0] = '\0';
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nq <= 0 || Nkv <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  // each token row holds its heads side by side, in whole 16-byte units
+  const long long lds[4] = {q_ld, k_ld, v_ld, o_ld};
+  const long long need[4] = {static_cast<long long>(Hq) * d, static_cast<long long>(Hkv) * d,
+                             static_cast<long long>(Hkv) * d, static_cast<long long>(Hq) * d};
+  for (int i = 0; i < 4; ++i)
+    if (lds[i] < need[i] || lds[i] % 8 != 0) return ATTN_ERR_INVALID_ARG;
+  // tensor-map strides stay below 2^40 bytes; query rows fit 32-bit indexing
+  if (2 * q_ld * B * Nq >= (1LL << 40) || 2 * k_ld * B * Nkv >= (1LL << 40) || 2 * v_ld * B * Nkv >= (1LL << 40))
+    return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * Hq * Nq >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
+  DeviceInfo* dev = nullptr;
+  int st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  const PrefillLayout lay{q_ld, k_ld, v_ld, o_ld};
+  float* o32 = o_fp32 ? static_cast<float*>(o) : nullptr;
+  uint16_t* o16 = o_fp32 ? nullptr : static_cast<uint16_t*>(o);
+  if ((st = run_prefill(q, k, v, o32, o16, lse, B, Hq, Hkv, Nq, Nkv, d, causal, scale * 1.4426950408889634f, lay,
+                        dev, stream)) != ATTN_OK)
+    return st;
+  if (check_env()) return read_device_error(stream, dev->err, 0);
+  return ATTN_OK;
+}
+
+int attn_layer_fwd(const void* x, const void* w_qkv, const void* w_o, void* qkv, void* o, void* y, float* lse, int B,
+                   int N, int d_model, int Hq, int Hkv, int d, int causal, float scale, int y_fp32,
+                   attn_stream_t stream) {
+  if (x == nullptr || w_qkv == nullptr || w_o == nullptr || qkv == nullptr || o == nullptr || y == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || N <= 0 || d_model <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  const long long tokens = static_cast<long long>(B) * N;
+  const long long nqkv = static_cast<long long>(Hq + 2 * Hkv) * d;
+  const long long nq = static_cast<long long>(Hq) * d;
+  if (tokens >= (1LL << 31) || nqkv >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
+  const uint16_t* base = static_cast<const uint16_t*>(qkv);
+  int st;
+  // QKV = X W_qkv^T: one token per row, the Q heads, then the K heads, then
+  // the V heads side by side
+  if ((st = gemm_bf16_nt(x, w_qkv, qkv, static_cast<int>(tokens), static_cast<int>(nqkv), d_model, 0, stream)) !=
+      ATTN_OK)
+    return st;
+  // attention straight on the GEMM's output rows; O token-major [B*N, Hq*d]
+  if ((st = attn_fwd_bshd(base, base + nq, base + nq + static_cast<long long>(Hkv) * d, o, lse, B, Hq, Hkv, N, N, d,
+                          nqkv, nqkv, nqkv, nq, 0, causal, scale, stream)) != ATTN_OK)
+    return st;
+  // Y = O W_o^T
+  return gemm_bf16_nt(o, w_o, y, static_cast<int>(tokens), d_model, static_cast<int>(nq), y_fp32, stream);
 }
 
 }  // extern "C"

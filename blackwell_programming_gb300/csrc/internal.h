@@ -13,8 +13,14 @@ namespace gbattn {
 struct PrefillParams {
   float* o;            // fp32 O, or null when o_bf16 is set
   uint16_t* o_bf16;    // bf16 O (same layout), or null
-  float* lse;          // may be null
+  float* lse;          // may be null; [B, Hq, Nq]
   int B, Hq, Hkv, Nq, Nkv, d_v;
+  // Layout of Q, K and V in their 4-D tensor maps: 0 = (features, rows,
+  // heads, batch), i.e. [B, H, N, d]; 1 = (features, heads, rows, batch),
+  // i.e. token-major [B, N, H, d] with any token stride.
+  int token_major;
+  // O element (b, h, row, c) is at o[b * o_sb + h * o_sh + row * o_sr + c].
+  long long o_sb, o_sh, o_sr;
   int causal;
   float scale_log2;    // scale * log2(e)
   int num_units;       // B * Hq * ceil(Nq / 256)

@@ -203,27 +203,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           qph ^= 1u << t;
           mbar_arrive_expect_tx(bar(C::B_QFULL + t), C::Q_BYTES);
           note_fill(t, ((qph >> t) & 1u) ^ 1u);
+          const int qrow = (U.qb * 2 + t) * BM;
           for (int kc = 0; kc < C::KCH; ++kc)
-            tma_load_3d(sQ + t * C::Q_BYTES + kc * C::CHUNK_Q, &tmQ, bar(C::B_QFULL + t), kc * 64,
-                        (U.qb * 2 + t) * BM, U.b * p.Hq + U.h, pol_q);
+            tma_load_4d(sQ + t * C::Q_BYTES + kc * C::CHUNK_Q, &tmQ, bar(C::B_QFULL + t), kc * 64,
+                        p.token_major ? U.h : qrow, p.token_major ? qrow : U.h, U.b, pol_q);
         }
         if (!ok) break;
         const int nmax = max(U.n[0], U.n[1]);
-        const int z = U.b * p.Hkv + U.h / group;
+        const int kvh = U.h / group;
         for (int j = 0; j < nmax && ok; ++j) {
           if (!(ok = mbar_wait(bar(C::B_KEMPTY + ks), kph ^ 1u, wctx))) break;
           mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::KV_BYTES);
           note_fill(2 + ks, kph);
           for (int kc = 0; kc < C::KCH; ++kc)
-            tma_load_3d(sK + ks * C::KV_BYTES + kc * C::CHUNK_KV, &tmK, bar(C::B_KFULL + ks), kc * 64, j * BN,
-                        z, pol_kv);
+            tma_load_4d(sK + ks * C::KV_BYTES + kc * C::CHUNK_KV, &tmK, bar(C::B_KFULL + ks), kc * 64,
+                        p.token_major ? kvh : j * BN, p.token_major ? j * BN : kvh, U.b, pol_kv);
           if (++ks == C::KS) { ks = 0; kph ^= 1u; }
           if (!(ok = mbar_wait(bar(C::B_VEMPTY + vs), vph ^ 1u, wctx))) break;
           mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::KV_BYTES);
           note_fill(2 + C::KS + vs, vph);
           for (int kc = 0; kc < C::KCH; ++kc)
-            tma_load_3d(sV + vs * C::KV_BYTES + kc * C::CHUNK_KV, &tmV, bar(C::B_VFULL + vs), kc * 64, j * BN,
-                        z, pol_kv);
+            tma_load_4d(sV + vs * C::KV_BYTES + kc * C::CHUNK_KV, &tmV, bar(C::B_VFULL + vs), kc * 64,
+                        p.token_major ? kvh : j * BN, p.token_major ? j * BN : kvh, U.b, pol_kv);
           if (++vs == C::VS) { vs = 0; vph ^= 1u; }
         }
         if (!ok) break;
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warp then writes 8 rows x 32 contiguous bytes (whole sectors),
       // instead of 32 rows x 16 bytes with one row per thread.
       // fp32 O, or bf16 O when the call asked for it (p.o_bf16)
-      const size_t ohead = static_cast<size_t>(U.b * p.Hq + U.h) * p.Nq * D;
+      const long long ohead = U.b * p.o_sb + U.h * p.o_sh;
       const bool bf = p.o_bf16 != nullptr;
 #pragma unroll 1
       for (int hl = 0; hl < 2; ++hl) {
@@ -481,8 +482,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float ia = __shfl_sync(kFull, inv_l, hl * 16 + (lane >> 2));
         const float ib = __shfl_sync(kFull, inv_l, hl * 16 + (lane >> 2) + 8);
         const bool la = q0 + ra < p.Nq, lb = q0 + ra + 8 < p.Nq;
-        const size_t oa = ohead + static_cast<size_t>(la ? q0 + ra : 0) * D + 2 * (lane & 3);
-        const size_t ob = ohead + static_cast<size_t>(lb ? q0 + ra + 8 : 0) * D + 2 * (lane & 3);
+        const long long oa = ohead + (la ? q0 + ra : 0) * p.o_sr + 2 * (lane & 3);
+        const long long ob = ohead + (lb ? q0 + ra + 8 : 0) * p.o_sr + 2 * (lane & 3);
 #pragma unroll 1
         for (int ch = 0; ch < D / 64; ++ch) {
           uint32_t r[32];
@@ -496,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 8; ++k) {
             const float a0 = __uint_as_float(r[4 * k]) * ia, a1 = __uint_as_float(r[4 * k + 1]) * ia;
             const float b0 = __uint_as_float(r[4 * k + 2]) * ib, b1 = __uint_as_float(r[4 * k + 3]) * ib;
-            const size_t c = static_cast<size_t>(ch * 64 + 8 * k);
+            const int c = ch * 64 + 8 * k;
             if (bf) {
               if (la) *reinterpret_cast<uint32_t*>(p.o_bf16 + oa + c) = pack_bf16x2(a0, a1);
               if (lb) *reinterpret_cast<uint32_t*>(p.o_bf16 + ob + c) = pack_bf16x2(b0, b1);

@@ -104,6 +104,37 @@ int attn_fwd_bf16out(const void* q, const void* k, const void* v, void* o, float
                      int causal, float scale, attn_stream_t stream);
 
 /*
+ * attn_fwd_bshd - attn_fwd (head dims 64 and 128) on token-major tensors:
+ * the layout in which a projection GEMM writes Q, K and V (one row per token,
+ * the heads side by side), so attention reads them in place and writes O in
+ * the layout the output projection reads ("CS149 L11: Programming
+ * Specialized Hardware", section 6: the Q/K/V GEMMs, attention and the O
+ * GEMM of one decoder layer).
+ *
+ *  q  bf16, element (b, h, i, c) at q[(b * Nq + i) * q_ld + h * d + c],
+ *     h < Hq, i < Nq, c < d.
+ *  k  bf16, element (b, g, j, c) at k[(b * Nkv + j) * k_ld + g * d + c],
+ *     g < Hkv.
+ *  v  bf16, same form with v_ld.
+ *  o  written, element (b, h, i, c) at o[(b * Nq + i) * o_ld + h * d + c]:
+ *     fp32 when o_fp32 != 0, else bf16 (each value rounded once, to nearest
+ *     even).  Elements of a row past Hq * d are not touched.  o must not
+ *     overlap q, k or v.
+ *  lse  fp32 [B, Hq, Nq] (head-major, as in attn_fwd), or NULL.
+ *  d is 64 or 128 (d_qk == d_v == d).  Each ld counts elements, is a multiple
+ *  of 8 and at least the heads' width (Hq * d for q and o, Hkv * d for k and
+ *  v); pointers are 16-byte aligned, so Q, K and V may be column slices of
+ *  one [B * N, (Hq + 2 * Hkv) * d] buffer.
+ *  Heads, GQA map, causal alignment, scale and errors as in attn_fwd;
+ *  ATTN_ERR_UNSUPPORTED for another d, or sizes past the tensor map's 2^40-byte
+ *  strides or 32-bit row indexing.
+ */
+int attn_fwd_bshd(const void* q, const void* k, const void* v, void* o, float* lse,
+                  int B, int Hq, int Hkv, int Nq, int Nkv, int d,
+                  long long q_ld, long long k_ld, long long v_ld, long long o_ld,
+                  int o_fp32, int causal, float scale, attn_stream_t stream);
+
+/*
  * attn_check_device - synchronise `stream` and read the device error word
  * that the kernels set when a bounded wait gives up (see
  * ATTN_ERR_TIMEOUT).  reset != 0 clears the word.  Returns ATTN_OK,
