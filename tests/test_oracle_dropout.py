@@ -1,0 +1,159 @@
+"""Pins for the dropout oracle and its counter-based generator, independent of
+the oracle's own code: the dropout-free special case, statistical properties
+of the generator's bits (balance, avalanche), the drop rate and the
+expectation of O within binomial / central-limit bounds, size independence of
+the masks, and a scalar pure-Python evaluator."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import attention
+from oracle.dropout_fp64 import (attention_dropout, drop_threshold, keep_mask, philox4x32_10,
+                                 uniforms16)
+
+
+def _inputs(r, B, Hq, Hkv, Nq, Nkv, d):
+    q = r.standard_normal((B, Hq, Nq, d))
+    k = r.standard_normal((B, Hkv, Nkv, d))
+    v = r.standard_normal((B, Hkv, Nkv, d))
+    return q, k, v
+
+
+def test_zero_probability_is_plain_attention():
+    r = np.random.default_rng(1)
+    q, k, v = _inputs(r, 2, 4, 2, 9, 13, 8)
+    for causal in (False, True):
+        o, lse = attention_dropout(q, k, v, causal, 0.4, 0.0, seed=1234)
+        o_ref, lse_ref = attention(q, k, v, causal, 0.4)
+        assert np.array_equal(o, o_ref) and np.array_equal(lse, lse_ref)
+
+
+def test_threshold_quantisation():
+    assert drop_threshold(0.0) == 0
+    assert drop_threshold(0.5) == 32768
+    assert drop_threshold(0.25) == 16384
+    assert drop_threshold(1.0 / 65536) == 1
+    assert drop_threshold(0.1) == 6554                 # 6553.6 rounds up
+    with pytest.raises(ValueError):
+        drop_threshold(1.0)
+
+
+def _bits(words):
+    return np.unpackbits(np.ascontiguousarray(words).view(np.uint8), axis=-1)
+
+
+def test_generator_bits_balanced_and_uniform():
+    n = 1 << 18
+    ctr = np.zeros((n, 4), dtype=np.uint64)
+    ctr[:, 0] = np.arange(n)
+    out = philox4x32_10(ctr, (0x12345678, 0x9ABCDEF0))
+    bits = _bits(out)                                  # [n, 128]
+    freq = bits.mean(axis=0)
+    sigma = 0.5 / math.sqrt(n)
+    assert np.all(np.abs(freq - 0.5) < 6 * sigma)
+    # top byte of each 16-bit half: 256 bins, chi-square with 255 degrees of freedom
+    u = np.concatenate([(out & 0xFFFF).ravel(), (out >> 16).ravel()]) >> 8
+    counts = np.bincount(u, minlength=256)
+    e = len(u) / 256
+    chi2 = float(((counts - e) ** 2 / e).sum())
+    assert 180 < chi2 < 340                            # about +-4.5 sigma around 255
+
+
+def test_generator_avalanche():
+    """Flipping any one bit of the counter or of the key flips half of the 128
+    output bits on average (a generator with too few or broken rounds fails)."""
+    r = np.random.default_rng(5)
+    n = 2048
+    base = r.integers(0, 1 << 32, size=(n, 4), dtype=np.uint64)
+    key = (0xDEADBEEF, 0x01234567)
+    ref = _bits(philox4x32_10(base, key))
+    for word in range(4):
+        for bit in range(32):
+            flipped = base.copy()
+            flipped[:, word] ^= np.uint64(1 << bit)
+            diff = (_bits(philox4x32_10(flipped, key)) != ref).sum(axis=1).mean()
+            assert 62.0 < diff < 66.0, (word, bit, diff)
+    for kw in range(2):
+        for bit in (0, 7, 31):
+            k2 = list(key)
+            k2[kw] ^= 1 << bit
+            diff = (_bits(philox4x32_10(base, tuple(k2))) != ref).sum(axis=1).mean()
+            assert 62.0 < diff < 66.0
+
+
+def test_drop_rate_binomial():
+    for p in (0.1, 0.5, 0.9):
+        t = drop_threshold(p)
+        keep = keep_mask(1, 3, np.arange(1000), 1000, seed=77, t=t)
+        n = keep.size
+        q = t / 65536.0
+        dropped = n - int(keep.sum())
+        assert abs(dropped - n * q) < 6 * math.sqrt(n * q * (1 - q))
+
+
+def test_masks_depend_only_on_position():
+    t = drop_threshold(0.3)
+    a = keep_mask(0, 2, np.arange(40), 100, seed=9, t=t)
+    b = keep_mask(0, 2, np.arange(10, 50), 333, seed=9, t=t)
+    assert np.array_equal(a[10:40], b[:30, :100])
+    # distinct rows, heads, batches and seeds draw distinct bits
+    base = uniforms16(0, 0, [5], 256, seed=1)
+    for other in (uniforms16(0, 0, [6], 256, 1), uniforms16(0, 1, [5], 256, 1),
+                  uniforms16(1, 0, [5], 256, 1), uniforms16(0, 0, [5], 256, 2),
+                  uniforms16(0, 0, [5], 256, 1 << 32)):
+        assert not np.array_equal(base, other)
+
+
+def test_expectation_is_dropout_free_output():
+    """Inverted dropout: averaged over seeds, O tends to the dropout-free O
+    (a missing or wrong rescale fails this by far)."""
+    r = np.random.default_rng(3)
+    q, k, v = _inputs(r, 1, 1, 1, 3, 24, 4)
+    o_ref, _ = attention(q, k, v, False, 0.5)
+    samples = np.stack([attention_dropout(q, k, v, False, 0.5, 0.4, seed=s)[0] for s in range(3000)])
+    mean = samples.mean(axis=0)
+    sem = samples.std(axis=0) / math.sqrt(len(samples))
+    assert np.all(np.abs(mean - o_ref) < 5 * sem + 1e-12)
+
+
+def _philox_scalar(c, k):
+    """Philox4x32-10 in plain integers, one counter at a time."""
+    c = [x & 0xFFFFFFFF for x in c]
+    k0, k1 = k
+    for _ in range(10):
+        a = 0xD2511F53 * c[0]
+        z = 0xCD9E8D57 * c[2]
+        c = [((z >> 32) ^ c[1] ^ k0) & 0xFFFFFFFF, z & 0xFFFFFFFF, ((a >> 32) ^ c[3] ^ k1) & 0xFFFFFFFF,
+             a & 0xFFFFFFFF]
+        k0 = (k0 + 0x9E3779B9) & 0xFFFFFFFF
+        k1 = (k1 + 0xBB67AE85) & 0xFFFFFFFF
+    return c
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_scalar_evaluator(causal):
+    B, Hq, Hkv, Nq, Nkv, d = 1, 2, 1, 5, 11, 3
+    r = np.random.default_rng(8 + causal)
+    q, k, v = _inputs(r, B, Hq, Hkv, Nq, Nkv, d)
+    p_drop, seed, scale = 0.35, (7 << 32) | 99, 0.6
+    o, _ = attention_dropout(q, k, v, causal, scale, p_drop, seed)
+    t = math.floor(float(np.float32(p_drop)) * 65536 + 0.5)
+    for h in range(Hq):
+        for i in range(Nq):
+            logits = {}
+            for j in range(Nkv):
+                if causal and j > i + Nkv - Nq:
+                    continue
+                logits[j] = scale * sum(q[0, h, i, c] * k[0, 0, j, c] for c in range(d))
+            mx = max(logits.values())
+            den = sum(math.exp(s - mx) for s in logits.values())
+            want = [0.0] * d
+            for j, s in logits.items():
+                word = _philox_scalar([j // 8, i, h, 0], (seed & 0xFFFFFFFF, seed >> 32))[(j % 8) // 2]
+                u = (word >> 16) if j % 2 else (word & 0xFFFF)
+                if u < t:
+                    continue
+                for c in range(d):
+                    want[c] += math.exp(s - mx) / den * v[0, 0, j, c] * 65536 / (65536 - t)
+            assert np.max(np.abs(o[0, h, i] - np.array(want))) < 1e-12
