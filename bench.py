@@ -171,13 +171,18 @@ def oracle_sample(wl, budget_s: float = 12.0):
     elapsed = 0.0
     while done < len(rng_heads):
         s = time.perf_counter()
-        attention_head(q[0, 0], k[0, 0], v[0, 0], wl.causal, wl.scale)
+        if DROPOUT > 0.0:
+            from oracle.dropout_fp64 import attention_dropout_head
+            attention_dropout_head(q[0, 0], k[0, 0], v[0, 0], wl.causal, wl.scale, DROPOUT, DROPOUT_SEED, 0, 0)
+        else:
+            attention_head(q[0, 0], k[0, 0], v[0, 0], wl.causal, wl.scale)
         elapsed += time.perf_counter() - s
         done += 1
         flops += per_head
         if elapsed >= budget_s or time.perf_counter() - t0 > 2 * budget_s:
             break
-    desc = "%d of %d (batch, head) pairs of %s, full rows, fp64 numpy" % (done, len(rng_heads), wl.name)
+    desc = "%d of %d (batch, head) pairs of %s, full rows, fp64 numpy%s" % (
+        done, len(rng_heads), wl.name, ", dropout %g" % DROPOUT if DROPOUT > 0.0 else "")
     return flops / elapsed / 1e12, desc, cores
 
 
@@ -227,6 +232,17 @@ def run_reference(args, wl):
 # O is written as fp32 (attn_fwd, the measured configuration) unless
 # --out bf16 selects attn_fwd_bf16out.
 O_DTYPE = "fp32"
+# Dropout probability on the softmax weights (--dropout; attn_fwd_dropout when > 0).
+DROPOUT = 0.0
+DROPOUT_SEED = 0x5EED
+
+
+def call_attn(q, k, v, wl, o, lse, stream):
+    import blackwell_programming_gb300 as gb
+    if DROPOUT > 0.0:
+        return gb.attn_fwd_dropout(q, k, v, DROPOUT, DROPOUT_SEED, causal=wl.causal, scale=wl.scale, out=o, lse=lse,
+                                   stream=stream)
+    return gb.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse, stream=stream)
 
 
 def o_torch_dtype():
@@ -245,7 +261,7 @@ def workload_config(wl):
             "d_qk": wl.d_qk, "d_v": wl.d_v, "causal": wl.causal, "scale": wl.scale,
             "inputs": "seeded N(0,1) bf16 (q x%g, k/v x%g)" % (wl.q_factor, wl.kv_factor),
             "l2": "flushed (256 MB write) before every step, outside the step events",
-            "parallelism": "replicas", "o_dtype": O_DTYPE}
+            "parallelism": "replicas", "o_dtype": O_DTYPE, "dropout": DROPOUT}
 
 
 def measure_device(wl, steps, warmup, world, stream, flush, inputs):
@@ -258,7 +274,7 @@ def measure_device(wl, steps, warmup, world, stream, flush, inputs):
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             flush.fill_(1.0)
-            gb.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse, stream=stream)
+            call_attn(q, k, v, wl, o, lse, stream)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         torch.cuda.synchronize()
         barrier(world)
@@ -266,7 +282,7 @@ def measure_device(wl, steps, warmup, world, stream, flush, inputs):
         for s, e in ev:
             flush.fill_(1.0)
             s.record(stream)
-            gb.attn_fwd(q, k, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse, stream=stream)
+            call_attn(q, k, v, wl, o, lse, stream)
             e.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -293,7 +309,7 @@ def measure_e2e(wl, steps, warmup, stream, host):
         if dv is not None:
             dv.copy_(hv, non_blocking=True)
         v = dv if dv is not None else dk[..., : wl.d_v]
-        gb.attn_fwd(dq, dk, v, causal=wl.causal, scale=wl.scale, out=o, lse=lse, stream=stream)
+        call_attn(dq, dk, v, wl, o, lse, stream)
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
@@ -373,7 +389,7 @@ def run_ours(args, wl):
                 "kernel": "latent_kernel (decode mode) + combine_kernel (one step)",
                 "algorithmic_bytes_per_launch": algorithmic_bytes(wl),
                 "tensor_tflops": flops / per_launch / 1e12}
-    roof["traffic"] = committed_traffic(kind, wl.name) if O_DTYPE == "fp32" else None
+    roof["traffic"] = committed_traffic(kind, wl.name) if O_DTYPE == "fp32" and DROPOUT == 0.0 else None
     launches = (2 if kind == "decode" else 1) * args.steps
 
     if rank == 0:
@@ -758,10 +774,14 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size (profiling cases)")
     ap.add_argument("--heads", type=int, default=None, help="override the workload's query heads (profiling cases)")
     ap.add_argument("--out", default="fp32", choices=["fp32", "bf16"], help="O output type (fp32 is the measured configuration)")
+    ap.add_argument("--dropout", type=float, default=0.0, help="dropout probability on the softmax weights (prefill shapes)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)      # at least three untimed warm-up steps
-    global O_DTYPE
+    global O_DTYPE, DROPOUT
     O_DTYPE = args.out
+    DROPOUT = args.dropout
+    if DROPOUT > 0.0 and O_DTYPE != "fp32":
+        ap.error("--dropout writes fp32 O")
     if args.workload in syn.GEMM_WORKLOADS:
         gw = syn.GEMM_WORKLOADS[args.workload]
         return run_gemm_reference(args, gw) if args.impl == "reference" else run_gemm_ours(args, gw)

@@ -12,7 +12,7 @@ from .binding import (ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG, ATTN_ERR_NO_DEVICE, A
                       attn_check_device, attn_decode_fwd_noalloc,
                       attn_decode_workspace_bytes, attn_fwd, attn_fwd_raw, attn_last_cuda_error,
                       attn_status_string,
-                      attn_version, attn_fwd_bshd, attn_layer_fwd, attn_layer_raw, gemm_nt, gemm_raw,
+                      attn_version, attn_fwd_bshd, attn_fwd_dropout, attn_layer_fwd, attn_layer_raw, gemm_nt, gemm_raw,
                       load_library)
 
 
@@ -27,4 +27,4 @@ __all__ = ["build", "attn_fwd", "attn_fwd_raw", "attn_check_device", "attn_statu
            "attn_version", "attn_decode_workspace_bytes", "attn_last_cuda_error", "AttnError", "load_library", "EXPORTS",
            "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_CUDA",
            "ATTN_ERR_TIMEOUT", "ATTN_ERR_NO_DEVICE", "ATTN_ERR_SCRATCH_LIMIT", "attn_decode_fwd_noalloc",
-           "gemm_nt", "gemm_raw", "attn_fwd_bshd", "attn_layer_fwd", "attn_layer_raw"]
+           "gemm_nt", "gemm_raw", "attn_fwd_bshd", "attn_layer_fwd", "attn_layer_raw", "attn_fwd_dropout"]

@@ -20,7 +20,7 @@ LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libgbattn.so")
 STAMP = os.path.join(LIBDIR, "host_arch.txt")
 SOURCES = ["attn_api.cu", "prefill_sm103.cu", "decode_sm103.cu", "gemm_sm103.cu"]
-HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "internal.h"),
+HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "philox.cuh"),
            os.path.join(ROOT, "include", "gbattn.h"), os.path.join(ROOT, "include", "gbgemm.h"),
            os.path.join(ROOT, "include", "gblayer.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -24,7 +24,7 @@ ATTN_ERR_SCRATCH_LIMIT = 6
 # Symbols the shared library exports (the declarations of include/gbattn.h).
 EXPORTS = ("attn_fwd", "attn_fwd_bf16out", "attn_check_device", "attn_status_string", "attn_last_cuda_error",
            "attn_version", "attn_decode_workspace_bytes", "attn_decode_fwd_noalloc", "gemm_bf16_nt",
-           "attn_fwd_bshd", "attn_layer_fwd")
+           "attn_fwd_bshd", "attn_layer_fwd", "attn_fwd_dropout")
 
 _lib = None
 
@@ -55,6 +55,8 @@ def load_library(path: str | None = None):
     L.attn_fwd_bshd.restype = i
     L.attn_layer_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
     L.attn_layer_fwd.restype = i
+    L.attn_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, f, ctypes.c_ulonglong, vp]
+    L.attn_fwd_dropout.restype = i
     L.gemm_bf16_nt.argtypes = [vp, vp, vp, i, i, i, i, vp]
     L.gemm_bf16_nt.restype = i
     L.attn_check_device.argtypes = [vp, i]
@@ -135,6 +137,46 @@ def attn_fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B
     return L.attn_fwd(ctypes.c_void_p(q_ptr), ctypes.c_void_p(k_ptr), ctypes.c_void_p(v_ptr),
                       ctypes.c_void_p(o_ptr), ctypes.c_void_p(lse_ptr), B, Hq, Hkv, Nq, Nkv, d_qk, d_v,
                       1 if causal else 0, ctypes.c_float(scale), ctypes.c_void_p(stream_ptr))
+
+
+def attn_fwd_dropout(q, k, v, p_drop: float, seed: int, causal: bool = False, scale: float | None = None,
+                     out=None, lse=None, want_lse: bool = True, stream=None):
+    """Attention with dropout on the softmax weights (attn_fwd_dropout in gbattn.h).
+
+    q: bf16 [B, Hq, Nq, d]; k, v: bf16 [B, Hkv, Nkv, d]; d 64 or 128, all
+    contiguous.  p_drop in [0, 1); seed: 64-bit integer.  Returns (o fp32
+    [B, Hq, Nq, d], lse fp32 [B, Hq, Nq] or None).
+    """
+    import torch
+    L = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 4:
+            raise TypeError("%s must be a 4-D bfloat16 CUDA tensor [B, H, N, d]" % name)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % name)
+    B, Hq, Nq, d = q.shape
+    _, Hkv, Nkv, _ = k.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[3] != d:
+        raise ValueError("shape mismatch: q %s k %s v %s" % (tuple(q.shape), tuple(k.shape), tuple(v.shape)))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = q.device
+    if out is None:
+        out = torch.empty((B, Hq, Nq, d), dtype=torch.float32, device=dev)
+    elif out.shape != (B, Hq, Nq, d) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous fp32 [B, Hq, Nq, d] tensor")
+    if want_lse and lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = L.attn_fwd_dropout(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                                ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(out.data_ptr()),
+                                ctypes.c_void_p(lse.data_ptr() if lse is not None else 0),
+                                B, Hq, Hkv, Nq, Nkv, d, d, 1 if causal else 0, ctypes.c_float(scale),
+                                ctypes.c_float(p_drop), ctypes.c_ulonglong(seed & 0xFFFFFFFFFFFFFFFF),
+                                _stream_handle(stream, dev))
+    if st != ATTN_OK:
+        _raise(L, st, "attn_fwd_dropout")
+    return out, lse
 
 
 def gemm_raw(a_ptr: int, b_ptr: int, c_ptr: int, M: int, N: int, K: int, c_fp32: bool,

@@ -242,10 +242,16 @@ struct PrefillLayout {
   long long q_ld, k_ld, v_ld, o_ld;
 };
 
+// Dropout of the prefill kernel: 16-bit threshold (0 = none) and seed.
+struct Dropout {
+  uint32_t t;
+  unsigned long long seed;
+};
+
 // The prefill kernel (d 64 or 128, d_v == d) on checked arguments.
 int run_prefill(const void* q, const void* k, const void* v, float* o32, uint16_t* o16, float* lse, int B, int Hq,
                 int Hkv, int Nq, int Nkv, int d, int causal, float scale_log2, const PrefillLayout& lay,
-                DeviceInfo* dev, cudaStream_t stream) {
+                const Dropout& drop, DeviceInfo* dev, cudaStream_t stream) {
   CUtensorMap tq, tk, tv;
   int st;
   if ((st = make_prefill_map(&tq, q, B, Hq, Nq, d, lay.q_ld)) != ATTN_OK) return st;
@@ -273,6 +279,10 @@ int run_prefill(const void* q, const void* k, const void* v, float* o32, uint16_
   }
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale_log2;
+  p.seed_lo = static_cast<uint32_t>(drop.seed & 0xFFFFFFFFull);
+  p.seed_hi = static_cast<uint32_t>(drop.seed >> 32);
+  p.drop_t = drop.t;
+  p.drop_scale = static_cast<float>(65536.0 / (65536.0 - static_cast<double>(drop.t)));
   p.nqb = (Nq + 255) / 256;
   p.nkv_tiles = (Nkv + 127) / 128;
   p.num_units = B * Hq * p.nqb;
@@ -283,9 +293,11 @@ int run_prefill(const void* q, const void* k, const void* v, float* o32, uint16_
   return ATTN_OK;
 }
 
-// attn_fwd and attn_fwd_bf16out: O is written as fp32 (o32) or bf16 (o16).
+// attn_fwd, attn_fwd_bf16out and attn_fwd_dropout: O is written as fp32
+// (o32) or bf16 (o16); `drop` is applied by the prefill kernel only.
 int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint16_t* o16, float* lse, int B, int Hq,
-                  int Hkv, int Nq, int Nkv, int d_qk, int d_v, int causal, float scale, attn_stream_t stream_) {
+                  int Hkv, int Nq, int Nkv, int d_qk, int d_v, int causal, float scale, attn_stream_t stream_,
+                  const Dropout& drop = Dropout{0u, 0ull}) {
   t_cuda_error[0] = '\0';
   const void* o = o32 != nullptr ? static_cast<const void*>(o32) : static_cast<const void*>(o16);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -305,6 +317,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint1
   const bool prefill = (d_qk == d_v) && (d_qk == 64 || d_qk == 128);
   const bool latent = (d_qk == 576 && d_v == 512);
   if (!prefill && !latent) return ATTN_ERR_UNSUPPORTED;
+  if (drop.t != 0u && !prefill) return ATTN_ERR_UNSUPPORTED;
   if (latent && !v_aliases_k) return ATTN_ERR_UNSUPPORTED;
   // One query per sequence sees every key under the bottom-right causal
   // alignment, so the causal flag changes nothing for the split-KV decode.
@@ -319,7 +332,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint1
 
   if (prefill) {
     const PrefillLayout lay{0, 0, 0, 0};
-    if ((st = run_prefill(q, k, v, o32, o16, lse, B, Hq, Hkv, Nq, Nkv, d_qk, causal, scale_log2, lay, dev,
+    if ((st = run_prefill(q, k, v, o32, o16, lse, B, Hq, Hkv, Nq, Nkv, d_qk, causal, scale_log2, lay, drop, dev,
                           stream)) != ATTN_OK)
       return st;
   } else if (!decode) {
@@ -434,6 +447,17 @@ int attn_fwd_bf16out(const void* q, const void* k, const void* v, void* o, float
                        scale, stream);
 }
 
+int attn_fwd_dropout(const void* q, const void* k, const void* v, float* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nkv, int d_qk, int d_v, int causal, float scale, float p_drop,
+                     unsigned long long seed, attn_stream_t stream) {
+  t_cuda_error[0] = '\0';
+  if (!(p_drop >= 0.f && p_drop < 1.f)) return ATTN_ERR_INVALID_ARG;   // also refuses NaN
+  const double tf = std::floor(static_cast<double>(p_drop) * 65536.0 + 0.5);
+  if (tf >= 65536.0) return ATTN_ERR_INVALID_ARG;                       // would drop every weight
+  const Dropout drop{static_cast<uint32_t>(tf), seed};
+  return attn_fwd_impl(q, k, v, o, nullptr, lse, B, Hq, Hkv, Nq, Nkv, d_qk, d_v, causal, scale, stream, drop);
+}
+
 int attn_fwd_bshd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
                   int Nkv, int d, long long q_ld, long long k_ld, long long v_ld, long long o_ld, int o_fp32,
                   int causal, float scale, attn_stream_t stream_) {
@@ -463,7 +487,7 @@ int attn_fwd_bshd(const void* q, const void* k, const void* v, void* o, float* l
   float* o32 = o_fp32 ? static_cast<float*>(o) : nullptr;
   uint16_t* o16 = o_fp32 ? nullptr : static_cast<uint16_t*>(o);
   if ((st = run_prefill(q, k, v, o32, o16, lse, B, Hq, Hkv, Nq, Nkv, d, causal, scale * 1.4426950408889634f, lay,
-                        dev, stream)) != ATTN_OK)
+                        Dropout{0u, 0ull}, dev, stream)) != ATTN_OK)
     return st;
   if (check_env()) return read_device_error(stream, dev->err, 0);
   return ATTN_OK;

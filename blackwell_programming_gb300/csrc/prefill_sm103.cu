@@ -35,6 +35,7 @@
 #include <cmath>
 
 #include "internal.h"
+#include "philox.cuh"
 #include "ptx.cuh"
 
 namespace gbattn {
@@ -123,7 +124,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
   return __all_sync(kFull, ok);
 }
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -383,6 +384,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
+        // Dropout keep bits of this row's 128 keys (bit c of keep[w] is key
+        // 32 w + c), drawn while the tensor core computes S: one generator
+        // call per 8 keys, 16 bits per key.
+        uint32_t keep[4] = {0u, 0u, 0u, 0u};
+        if constexpr (DROP) {
+#pragma unroll 1
+          for (int g = 0; g < BN / 8; ++g) {
+            const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j * (BN / 8) + g),
+                                                     static_cast<uint32_t>(row), static_cast<uint32_t>(U.h),
+                                                     static_cast<uint32_t>(U.b)),
+                                          p.seed_lo, p.seed_hi);
+            const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
+            uint32_t bits = 0u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              bits |= static_cast<uint32_t>((w4[q] & 0xFFFFu) >= p.drop_t) << (2 * q);
+              bits |= static_cast<uint32_t>((w4[q] >> 16) >= p.drop_t) << (2 * q + 1);
+            }
+            const uint32_t sh = bits << (8 * (g & 3));
+            const int wsel = g >> 2;
+            keep[0] |= wsel == 0 ? sh : 0u;
+            keep[1] |= wsel == 1 ? sh : 0u;
+            keep[2] |= wsel == 2 ? sh : 0u;
+            keep[3] |= wsel == 3 ? sh : 0u;
+          }
+        }
         if (!(ok = warp_wait(bar(C::B_SFULL + t), sph, wctx))) break;
         sph ^= 1u;
         tc_fence_after();
@@ -449,9 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < BN / 4; ++i) {
             const int e = h * (BN / 4) + i;
             const uint64_t x = f2_fma(f2_pack(v[2 * e], v[2 * e + 1]), c2, nb2);
-            const float p0 = ex2(f2_lo(x));
-            const float p1 = ex2(f2_hi(x));
+            float p0 = ex2(f2_lo(x));
+            float p1 = ex2(f2_hi(x));
             acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+            if constexpr (DROP) {
+              // dropout after the row sum: the normaliser counts every key,
+              // P V sees only the kept ones
+              if (!((keep[(2 * e) >> 5] >> ((2 * e) & 31)) & 1u)) p0 = 0.f;
+              if (!((keep[(2 * e + 1) >> 5] >> ((2 * e + 1) & 31)) & 1u)) p1 = 0.f;
+            }
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st32u(tS + h * (BN / 4), pk);
@@ -469,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ofph ^= 1u;
       tc_fence_after();
       const bool live = row < p.Nq;
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const float inv_l = (l > 0.f) ? (DROP ? p.drop_scale : 1.f) / l : 0.f;
       // O leaves TMEM in the 16x256b shape: each store instruction of the
       // warp then writes 8 rows x 32 contiguous bytes (whole sectors),
       // instead of 32 rows x 16 bytes with one row per thread.
@@ -526,11 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool DROP>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                      int num_sms, cudaStream_t stream) {
   using C = Cfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   const int grid = min(p.num_units, num_sms);
@@ -538,9 +571,9 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   // The register split needs the kernel to be launched with enough registers;
   // otherwise setmaxnreg.inc could never be served, so refuse to launch.
   cudaFuncAttributes fa;
-  if ((e = cudaFuncGetAttributes(&fa, prefill_kernel<D>)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, prefill_kernel<D, DROP>)) != cudaSuccess) return e;
   if (((fa.numRegs + 7) / 8) * 8 < kRegsNeededAtLaunch) return cudaErrorInvalidConfiguration;
-  prefill_kernel<D><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  prefill_kernel<D, DROP><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -548,8 +581,11 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int num_sms, cudaStream_t stream) {
-  if (d == 64) return launch_d<64>(tq, tk, tv, p, num_sms, stream);
-  if (d == 128) return launch_d<128>(tq, tk, tv, p, num_sms, stream);
+  const bool drop = p.drop_t != 0u;
+  if (d == 64) return drop ? launch_d<64, true>(tq, tk, tv, p, num_sms, stream)
+                           : launch_d<64, false>(tq, tk, tv, p, num_sms, stream);
+  if (d == 128) return drop ? launch_d<128, true>(tq, tk, tv, p, num_sms, stream)
+                            : launch_d<128, false>(tq, tk, tv, p, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -104,6 +104,33 @@ int attn_fwd_bf16out(const void* q, const void* k, const void* v, void* o, float
                      int causal, float scale, attn_stream_t stream);
 
 /*
+ * attn_fwd_dropout - attn_fwd with dropout on the softmax weights, the stage
+ * between Softmax and x V in the FlashAttention pipeline on "CS149 L11:
+ * Programming Specialized Hardware", section 5 (the training forward).
+ *
+ *   O = (P * Keep) V * 65536 / (65536 - t),  P = softmax(mask(scale Q K^T)),
+ *   t = floor(p_drop * 65536 + 1/2),
+ *
+ * where Keep[b, h, i, j] is 1 iff the 16-bit uniform of key j of query row i
+ * (its position in the sequence) in head h of batch b is >= t.  That uniform
+ * is half (j & 1) (the low half for even j) of word ((j >> 1) & 3) of
+ * Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC 2011) at counter
+ * (j >> 3, i, h, b) and key (seed mod 2^32, seed >> 32): a pure function of
+ * the position and the seed, so a backward pass can redraw the same mask.
+ * The realised drop probability is t / 65536 and the scale keeps E[O] equal
+ * to attn_fwd's O.  LSE is attn_fwd's (dropout does not change it).
+ *
+ * Arguments, layouts and errors as attn_fwd, O fp32, for the prefill shapes
+ * (d_qk == d_v, 64 or 128); ATTN_ERR_UNSUPPORTED for the latent shape and
+ * ATTN_ERR_INVALID_ARG unless 0 <= p_drop and t < 65536.  p_drop == 0 runs
+ * the same kernel as attn_fwd.
+ */
+int attn_fwd_dropout(const void* q, const void* k, const void* v, float* o, float* lse,
+                     int B, int Hq, int Hkv, int Nq, int Nkv, int d_qk, int d_v,
+                     int causal, float scale, float p_drop, unsigned long long seed,
+                     attn_stream_t stream);
+
+/*
  * attn_fwd_bshd - attn_fwd (head dims 64 and 128) on token-major tensors:
  * the layout in which a projection GEMM writes Q, K and V (one row per token,
  * the heads side by side), so attention reads them in place and writes O in

@@ -76,7 +76,10 @@ def drop_threshold(p: float) -> int:
     p32 = float(np.float32(p))
     if not 0.0 <= p32 < 1.0:
         raise ValueError("dropout probability must be in [0, 1)")
-    return int(np.floor(p32 * 65536.0 + 0.5))
+    t = int(np.floor(p32 * 65536.0 + 0.5))
+    if t >= 65536:
+        raise ValueError("dropout probability rounds to dropping every weight")
+    return t
 
 
 def uniforms16(b: int, h: int, rows, n_keys: int, seed: int) -> np.ndarray:

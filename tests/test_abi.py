@@ -114,3 +114,48 @@ def test_gemm_invalid_arguments(lib, bad):
 
 def test_gemm_sizes_past_32_bit_rows(lib):
     assert gb.gemm_raw(P, P * 2, P * 3, 1 << 20, 4096, 4096, False) == gb.ATTN_ERR_UNSUPPORTED
+
+
+def _dropout_raw(lib, p_drop, d_qk=128, d_v=128, v_ptr=P * 3):
+    import ctypes
+    return lib.attn_fwd_dropout(ctypes.c_void_p(P), ctypes.c_void_p(P * 2), ctypes.c_void_p(v_ptr),
+                                ctypes.c_void_p(P * 4), ctypes.c_void_p(P * 5), 1, 2, 1, 128, 128, d_qk, d_v, 0,
+                                ctypes.c_float(0.1), ctypes.c_float(p_drop), ctypes.c_ulonglong(7), None)
+
+
+@pytest.mark.parametrize("p_drop", [1.0, -0.1, float("nan"), 0.99999994, 2.0])
+def test_dropout_probability_checked(lib, p_drop):
+    # 0.99999994 is below 1 but rounds to t = 65536, which would drop every weight
+    assert _dropout_raw(lib, p_drop) == gb.ATTN_ERR_INVALID_ARG
+
+
+def test_dropout_latent_shape_unsupported(lib):
+    assert _dropout_raw(lib, 0.1, d_qk=576, d_v=512, v_ptr=P * 2) == gb.ATTN_ERR_UNSUPPORTED
+
+
+def _bshd_raw(lib, q=P, d=128, H=2, q_ld=256, k_ld=256, v_ld=256, o_ld=256):
+    import ctypes
+    return lib.attn_fwd_bshd(ctypes.c_void_p(q), ctypes.c_void_p(P * 2), ctypes.c_void_p(P * 3),
+                             ctypes.c_void_p(P * 4), None, 1, H, H, 64, 64, d, q_ld, k_ld, v_ld, o_ld, 0, 1,
+                             ctypes.c_float(0.1), None)
+
+
+@pytest.mark.parametrize("bad", [dict(q_ld=252), dict(k_ld=260), dict(o_ld=128), dict(v_ld=0), dict(q=P + 8)])
+def test_bshd_invalid_arguments(lib, bad):
+    assert _bshd_raw(lib, **bad) == gb.ATTN_ERR_INVALID_ARG
+
+
+def test_bshd_unsupported_head_dim(lib):
+    assert _bshd_raw(lib, d=96, q_ld=192, k_ld=192, v_ld=192, o_ld=192) == gb.ATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("bad,want", [
+    (dict(x=0), gb.ATTN_ERR_INVALID_ARG), (dict(y=0), gb.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3), gb.ATTN_ERR_INVALID_ARG), (dict(N=0), gb.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), gb.ATTN_ERR_UNSUPPORTED),
+])
+def test_layer_invalid_arguments(lib, bad, want):
+    a = dict(x=P, w_qkv=P * 2, w_o=P * 3, qkv=P * 4, o=P * 5, y=P * 6, B=1, N=64, d_model=256, Hq=4, Hkv=2, d=64)
+    a.update(bad)
+    assert gb.attn_layer_raw(a["x"], a["w_qkv"], a["w_o"], a["qkv"], a["o"], a["y"], 0, a["B"], a["N"],
+                             a["d_model"], a["Hq"], a["Hkv"], a["d"], True, 0.1, False) == want

@@ -37,6 +37,8 @@ def test_threshold_quantisation():
     assert drop_threshold(0.1) == 6554                 # 6553.6 rounds up
     with pytest.raises(ValueError):
         drop_threshold(1.0)
+    with pytest.raises(ValueError):
+        drop_threshold(0.99999994)                     # below 1, but t would be 65536
 
 
 def _bits(words):
