@@ -165,6 +165,11 @@ int make_prefill_map(CUtensorMap* m, const void* base, int B, int H, int N, int 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool env_flag(const char* name) {
+  const char* s = std::getenv(name);
+  return s != nullptr && s[0] == '1';
+}
+
 bool check_env() {
   static const bool on = [] {
     const char* s = std::getenv("ATTN_CHECK");
@@ -422,20 +427,24 @@ int gemm_bf16_nt(const void* a, const void* b, void* c, int M, int N, int K, int
   if (st != ATTN_OK) return st;
   CUtensorMap ta, tb;
   const uint64_t rs = static_cast<uint64_t>(K) * 2;
+  const bool use_pair = gemm_use_pair(M) && !env_flag("ATTN_GEMM_SINGLE_CTA");
   if ((st = make_map(&ta, a, K, M, 1, rs, rs * M, gemm_tile_rows())) != ATTN_OK) return st;
-  if ((st = make_map(&tb, b, K, N, 1, rs, rs * N, gemm_tile_cols())) != ATTN_OK) return st;
+  if ((st = make_map(&tb, b, K, N, 1, rs, rs * N, gemm_b_box_rows(use_pair))) != ATTN_OK) return st;
   GemmParams p{};
   p.c = c;
   p.M = M;
   p.N = N;
   p.K = K;
   p.c_fp32 = c_fp32 ? 1 : 0;
-  p.tiles_m = (M + gemm_tile_rows() - 1) / gemm_tile_rows();
+  const int rows_per_tile = use_pair ? 2 * gemm_tile_rows() : gemm_tile_rows();
+  p.tiles_m = (M + rows_per_tile - 1) / rows_per_tile;
   p.tiles_n = (N + gemm_tile_cols() - 1) / gemm_tile_cols();
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.err = dev->err;
   cudaError_t e;
-  if ((e = launch_gemm(ta, tb, p, dev->num_sms, stream)) != cudaSuccess) return cuda_fail(e, "gemm launch");
+  if ((e = use_pair ? launch_gemm_pair(ta, tb, p, dev->num_sms, stream) : launch_gemm(ta, tb, p, dev->num_sms, stream)) !=
+      cudaSuccess)
+    return cuda_fail(e, "gemm launch");
   if (check_env()) return read_device_error(stream, dev->err, 0);
   return ATTN_OK;
 }

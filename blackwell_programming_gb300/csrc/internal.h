@@ -101,6 +101,13 @@ struct GemmParams {
 int gemm_tile_rows();
 int gemm_tile_cols();
 int gemm_tile_depth();
+// CTA-pair GEMM (256 x 256 tiles over two SMs), chosen for M > 128.  Its B
+// map takes boxes of gemm_b_box_rows(true) rows; tiles_m counts 256-row
+// blocks.
+bool gemm_use_pair(int M);
+int gemm_b_box_rows(bool use_pair);
+cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int num_sms,
+                             cudaStream_t stream);
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int num_sms,
                         cudaStream_t stream);
 

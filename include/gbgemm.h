@@ -30,6 +30,10 @@ extern "C" {
  *  tensor-memory-accelerator rule) and N % 2 == 0.  Pointers 16-byte
  *  aligned.
  *
+ * For M > 128 the two CTAs of a thread-block cluster share each 256 x 256
+ * output tile (the environment variable ATTN_GEMM_SINGLE_CTA=1 selects the
+ * one-CTA kernel with 128 x 256 tiles instead, for comparison).
+ *
  * Returns ATTN_OK once the kernel is enqueued, ATTN_ERR_INVALID_ARG for a
  * null or misaligned pointer or a size outside the rules above,
  * ATTN_ERR_UNSUPPORTED for sizes past 32-bit row indexing, ATTN_ERR_CUDA /

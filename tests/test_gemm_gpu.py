@@ -80,3 +80,27 @@ def test_gemm_full_size_sampled_and_deterministic(gb):
     ref = gemm_nt_rows(a64, b64, range(len(rows)))
     bound = K * 2.0 ** -24 * (np.abs(a64) @ np.abs(b64).T)
     assert float(np.max(np.abs(c - ref) - bound)) <= 0.0
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 520, 136), (2048, 768, 4096), (129, 256, 64), (256, 6, 8), (4096, 4096, 512)])
+def test_pair_and_single_cta_kernels_agree(gb, M, N, K, monkeypatch):
+    """M > 128 runs the CTA-pair kernel; ATTN_GEMM_SINGLE_CTA=1 forces the
+    one-CTA kernel.  Both meet the bound; they sum each element's K products
+    in the same 16-deep steps, so they agree to the last bit."""
+    a, b = make_ab(M, N, K, seed=3 * M + N + K)
+    da, db = to_dev(a), to_dev(b)
+    gb.attn_check_device(reset=True)
+    c_pair = gb.gemm_nt(da, db, out_dtype=torch.float32)
+    monkeypatch.setenv("ATTN_GEMM_SINGLE_CTA", "1")
+    c_single = gb.gemm_nt(da, db, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert gb.attn_check_device(reset=True) == 0
+    a64, b64 = syn.bf16_bits_to_f64(a), syn.bf16_bits_to_f64(b)
+    if M * N * K <= 2048 * 768 * 4096:
+        check_fp32(c_pair.cpu().numpy(), a64, b64, "pair")
+    else:
+        rows = list(range(0, M, 97))
+        ref = gemm_nt_rows(a64, b64, rows)
+        bound = K * 2.0 ** -24 * (np.abs(a64[rows]) @ np.abs(b64).T)
+        assert float(np.max(np.abs(c_pair.cpu().numpy()[rows] - ref) - bound)) <= 0.0
+    assert torch.equal(c_pair, c_single)
