@@ -247,7 +247,7 @@ struct PrefillLayout {
   long long q_ld, k_ld, v_ld, o_ld;
 };
 
-// Dropout of the prefill kernel: 16-bit threshold (0 = none) and seed.
+// Dropout of the prefill kernel: 8-bit threshold (0 = none) and seed.
 struct Dropout {
   uint32_t t;
   unsigned long long seed;
@@ -287,7 +287,7 @@ int run_prefill(const void* q, const void* k, const void* v, float* o32, uint16_
   p.seed_lo = static_cast<uint32_t>(drop.seed & 0xFFFFFFFFull);
   p.seed_hi = static_cast<uint32_t>(drop.seed >> 32);
   p.drop_t = drop.t;
-  p.drop_scale = static_cast<float>(65536.0 / (65536.0 - static_cast<double>(drop.t)));
+  p.drop_scale = static_cast<float>(256.0 / (256.0 - static_cast<double>(drop.t)));
   p.nqb = (Nq + 255) / 256;
   p.nkv_tiles = (Nkv + 127) / 128;
   p.num_units = B * Hq * p.nqb;
@@ -461,8 +461,8 @@ int attn_fwd_dropout(const void* q, const void* k, const void* v, float* o, floa
                      unsigned long long seed, attn_stream_t stream) {
   t_cuda_error[0] = '\0';
   if (!(p_drop >= 0.f && p_drop < 1.f)) return ATTN_ERR_INVALID_ARG;   // also refuses NaN
-  const double tf = std::floor(static_cast<double>(p_drop) * 65536.0 + 0.5);
-  if (tf >= 65536.0) return ATTN_ERR_INVALID_ARG;                       // would drop every weight
+  const double tf = std::floor(static_cast<double>(p_drop) * 256.0 + 0.5);
+  if (tf >= 256.0) return ATTN_ERR_INVALID_ARG;                         // would drop every weight
   const Dropout drop{static_cast<uint32_t>(tf), seed};
   return attn_fwd_impl(q, k, v, o, nullptr, lse, B, Hq, Hkv, Nq, Nkv, d_qk, d_v, causal, scale, stream, drop);
 }

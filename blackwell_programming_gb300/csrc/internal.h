@@ -24,10 +24,10 @@ struct PrefillParams {
   int causal;
   float scale_log2;    // scale * log2(e)
   // Dropout on P (drop_t == 0: none).  Key j of query row i in head (b, h)
-  // is dropped iff its 16-bit uniform is below drop_t; the uniform is half
-  // (j & 1) of word ((j >> 1) & 3) of Philox4x32-10 at counter
-  // (j >> 3, i, h, b) and key (seed_lo, seed_hi).  Kept weights are scaled
-  // by drop_scale = 65536 / (65536 - drop_t) in the epilogue.
+  // is dropped iff its 8-bit uniform is below drop_t; the uniform is byte
+  // (j & 3) of word ((j >> 2) & 3) of Philox4x32-10 at counter
+  // (j >> 4, i, h, b) and key (seed_lo, seed_hi).  Kept weights are scaled
+  // by drop_scale = 256 / (256 - drop_t) in the epilogue.
   uint32_t seed_lo, seed_hi, drop_t;
   float drop_scale;
   int num_units;       // B * Hq * ceil(Nq / 256)

@@ -386,12 +386,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n; ++j) {
         // Dropout keep bits of this row's 128 keys (bit c of keep[w] is key
         // 32 w + c), drawn while the tensor core computes S: one generator
-        // call per 8 keys, 16 bits per key.
+        // call per 16 keys, one byte per key.  A byte u is kept iff
+        // u >= t, i.e. iff u + (256 - t) carries into bit 8: two bytes at a
+        // time in 16-bit lanes that cannot overflow.
         uint32_t keep[4] = {0u, 0u, 0u, 0u};
         if constexpr (DROP) {
+          const uint32_t c2 = (256u - p.drop_t) * 0x00010001u;
 #pragma unroll 1
-          for (int g = 0; g < BN / 8; ++g) {
-            const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j * (BN / 8) + g),
+          for (int g = 0; g < BN / 16; ++g) {
+            const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j * (BN / 16) + g),
                                                      static_cast<uint32_t>(row), static_cast<uint32_t>(U.h),
                                                      static_cast<uint32_t>(U.b)),
                                           p.seed_lo, p.seed_hi);
@@ -399,11 +402,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t bits = 0u;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              bits |= static_cast<uint32_t>((w4[q] & 0xFFFFu) >= p.drop_t) << (2 * q);
-              bits |= static_cast<uint32_t>((w4[q] >> 16) >= p.drop_t) << (2 * q + 1);
+              const uint32_t ev = (w4[q] & 0x00FF00FFu) + c2;          // bytes 0 and 2
+              const uint32_t od = ((w4[q] >> 8) & 0x00FF00FFu) + c2;   // bytes 1 and 3
+              const uint32_t nib = ((ev >> 8) & 1u) | ((od >> 7) & 2u) | ((ev >> 22) & 4u) | ((od >> 21) & 8u);
+              bits |= nib << (4 * q);
             }
-            const uint32_t sh = bits << (8 * (g & 3));
-            const int wsel = g >> 2;
+            const uint32_t sh = bits << (16 * (g & 1));
+            const int wsel = g >> 1;
             keep[0] |= wsel == 0 ? sh : 0u;
             keep[1] |= wsel == 1 ? sh : 0u;
             keep[2] |= wsel == 2 ? sh : 0u;

@@ -108,21 +108,23 @@ int attn_fwd_bf16out(const void* q, const void* k, const void* v, void* o, float
  * between Softmax and x V in the FlashAttention pipeline on "CS149 L11:
  * Programming Specialized Hardware", section 5 (the training forward).
  *
- *   O = (P * Keep) V * 65536 / (65536 - t),  P = softmax(mask(scale Q K^T)),
- *   t = floor(p_drop * 65536 + 1/2),
+ *   O = (P * Keep) V * 256 / (256 - t),  P = softmax(mask(scale Q K^T)),
+ *   t = floor(p_drop * 256 + 1/2),
  *
- * where Keep[b, h, i, j] is 1 iff the 16-bit uniform of key j of query row i
+ * where Keep[b, h, i, j] is 1 iff the 8-bit uniform of key j of query row i
  * (its position in the sequence) in head h of batch b is >= t.  That uniform
- * is half (j & 1) (the low half for even j) of word ((j >> 1) & 3) of
- * Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC 2011) at counter
- * (j >> 3, i, h, b) and key (seed mod 2^32, seed >> 32): a pure function of
- * the position and the seed, so a backward pass can redraw the same mask.
- * The realised drop probability is t / 65536 and the scale keeps E[O] equal
- * to attn_fwd's O.  LSE is attn_fwd's (dropout does not change it).
+ * is byte (j & 3) (the least significant for j & 3 = 0) of word
+ * ((j >> 2) & 3) of Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC 2011) at
+ * counter (j >> 4, i, h, b) and key (seed mod 2^32, seed >> 32): a pure
+ * function of the position and the seed, so a backward pass can redraw the
+ * same mask.  The realised drop probability is t / 256 and the scale keeps
+ * E[O] equal to attn_fwd's O.  LSE is attn_fwd's (dropout does not change
+ * it).
  *
  * Arguments, layouts and errors as attn_fwd, O fp32, for the prefill shapes
  * (d_qk == d_v, 64 or 128); ATTN_ERR_UNSUPPORTED for the latent shape and
- * ATTN_ERR_INVALID_ARG unless 0 <= p_drop and t < 65536.  p_drop == 0 runs
+ * ATTN_ERR_INVALID_ARG unless 0 <= p_drop and t < 256.  p_drop == 0 (or any
+ * p_drop < 1/512, which rounds to t = 0) runs
  * the same kernel as attn_fwd.
  */
 int attn_fwd_dropout(const void* q, const void* k, const void* v, float* o, float* lse,

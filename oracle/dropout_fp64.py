@@ -22,13 +22,13 @@ Readings where the pages are silent (the slide names the stage only):
   (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
   SC 2011), so any element's bits can be drawn on their own.  For key j of
   query row i (its position in the sequence) in head h of batch b, with a
-  64-bit seed: counter (j >> 3, i, h, b), key (seed mod 2^32, seed >> 32);
-  the element's 16-bit uniform is half (j & 1) (the low half for even j) of
-  output word ((j >> 1) & 3).
-* The probability is quantised to 16 bits: t = floor(p * 65536 + 1/2); the
+  64-bit seed: counter (j >> 4, i, h, b), key (seed mod 2^32, seed >> 32);
+  the element's 8-bit uniform is byte (j & 3) (the least significant for
+  j & 3 = 0) of output word ((j >> 2) & 3), so one call serves 16 keys.
+* The probability is quantised to 8 bits: t = floor(p * 256 + 1/2); the
   element is dropped iff its uniform is below t, so the realised drop
-  probability is t / 65536, and kept weights are scaled by
-  65536 / (65536 - t), which keeps the expectation exact.
+  probability is t / 256, and kept weights are scaled by 256 / (256 - t),
+  which keeps the expectation exact.
 
 Pinned by tests/test_oracle_dropout.py: p = 0 is plain attention, the
 generator's output bits are balanced and every input bit avalanches, the drop
@@ -70,38 +70,45 @@ def philox4x32_10(ctr, key):
     return np.stack([c0, c1, c2, c3], axis=-1).astype(np.uint32)
 
 
+KEEP_LEVELS = 256   # the uniforms have 8 bits
+
+
 def drop_threshold(p: float) -> int:
-    """The 16-bit threshold t for drop probability p (0 <= p < 1), computed
+    """The 8-bit threshold t for drop probability p (0 <= p < 1), computed
     from p as a float32 value, as a C caller passes it."""
     p32 = float(np.float32(p))
     if not 0.0 <= p32 < 1.0:
         raise ValueError("dropout probability must be in [0, 1)")
-    t = int(np.floor(p32 * 65536.0 + 0.5))
-    if t >= 65536:
+    t = int(np.floor(p32 * KEEP_LEVELS + 0.5))
+    if t >= KEEP_LEVELS:
         raise ValueError("dropout probability rounds to dropping every weight")
     return t
 
 
-def uniforms16(b: int, h: int, rows, n_keys: int, seed: int) -> np.ndarray:
-    """The 16-bit uniforms [len(rows), n_keys] of keys 0..n_keys-1 of the given
+def keep_scale(t: int) -> float:
+    """Factor on kept weights: the inverse of the realised keep probability."""
+    return KEEP_LEVELS / (KEEP_LEVELS - t)
+
+
+def uniforms8(b: int, h: int, rows, n_keys: int, seed: int) -> np.ndarray:
+    """The 8-bit uniforms [len(rows), n_keys] of keys 0..n_keys-1 of the given
     query rows of head h in batch b."""
     rows = np.asarray(rows, dtype=np.int64)
-    blocks = (n_keys + 7) // 8
+    blocks = (n_keys + 15) // 16
     ctr = np.zeros((len(rows), blocks, 4), dtype=np.uint64)
     ctr[..., 0] = np.arange(blocks)[None, :]
     ctr[..., 1] = rows[:, None]
     ctr[..., 2] = h
     ctr[..., 3] = b
     words = philox4x32_10(ctr, (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF))   # [R, blocks, 4]
-    lo = words & np.uint32(0xFFFF)
-    hi = words >> np.uint32(16)
-    u = np.stack([lo, hi], axis=-1).reshape(len(rows), blocks * 8)   # key 8*blk + 2*word + half
+    by = np.stack([(words >> np.uint32(8 * i)) & np.uint32(0xFF) for i in range(4)], axis=-1)
+    u = by.reshape(len(rows), blocks * 16)   # key 16*blk + 4*word + byte
     return u[:, :n_keys]
 
 
 def keep_mask(b: int, h: int, rows, n_keys: int, seed: int, t: int) -> np.ndarray:
     """True where the weight of (row, key) is kept."""
-    return uniforms16(b, h, rows, n_keys, seed) >= t
+    return uniforms8(b, h, rows, n_keys, seed) >= t
 
 
 def attention_dropout_head(q, k, v, causal: bool, scale: float, p_drop: float, seed: int, b: int, h: int,
@@ -118,7 +125,7 @@ def attention_dropout_head(q, k, v, causal: bool, scale: float, p_drop: float, s
     _, lse, p = attention_head(q, k, v, causal, scale, row_index=row_index, n_q=n_q, return_p=True)
     t = drop_threshold(p_drop)
     keep = keep_mask(b, h, row_index, n, seed, t)
-    o = (np.where(keep, p, 0.0) @ np.asarray(v, dtype=np.float64)) * (65536.0 / (65536.0 - t))
+    o = (np.where(keep, p, 0.0) @ np.asarray(v, dtype=np.float64)) * keep_scale(t)
     return o, lse
 
 

@@ -6,7 +6,7 @@ dropout oracle.
   key j0 + c, which is zero exactly when the kernel dropped it (the weights
   themselves stay far above bf16's smallest normal).
 * O with random V meets the attention bar scaled by the dropout factor
-  65536 / (65536 - t): the kernel's errors (bf16 P, fp32 sums) scale with the
+  256 / (256 - t): the kernel's errors (bf16 P, fp32 sums) scale with the
   weights it sums, and the kept ones are multiplied by that factor.
 * LSE is the dropout-free LSE: bit for bit attn_fwd's.
 """
@@ -15,6 +15,7 @@ import pytest
 
 from blackwell_programming_gb300 import synthetic as syn
 from oracle import attention_dropout, attention_dropout_rows, drop_threshold, keep_mask
+from oracle.dropout_fp64 import keep_scale
 from parity_util import LSE_REL, O_MAX_ABS, O_MEAN_ABS
 
 pytestmark = pytest.mark.gpu
@@ -102,7 +103,7 @@ def test_dropout_parity(gb, case):
     q64, k64, v64 = inp.f64()
     o_or, lse_or = attention_dropout(q64, k64, v64, causal, wl.scale, p_drop, SEED)
     t = drop_threshold(p_drop)
-    f = 65536.0 / (65536.0 - t)
+    f = keep_scale(t)
     err = np.abs(o.cpu().numpy() - o_or)
     assert float(err.max()) <= O_MAX_ABS * f, "max |dO| %.3e" % err.max()
     assert float(err.mean()) <= O_MEAN_ABS * f, "mean |dO| %.3e" % err.mean()
@@ -123,7 +124,7 @@ def test_dropout_full_size_sampled(gb):
     status_ok(gb)
     assert torch.equal(lse, lse0)
     q64, k64, v64 = inp.f64()
-    f = 65536.0 / (65536.0 - drop_threshold(0.1))
+    f = keep_scale(drop_threshold(0.1))
     rows = [0, 1, 127, 128, 255, 2047, 3000, 4095]
     for b, h in ((0, 0), (3, 31), (1, 17)):
         o_or, _ = attention_dropout_rows(q64, k64, v64, True, wl.scale, 0.1, SEED, b, h, rows)

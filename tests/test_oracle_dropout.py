@@ -9,8 +9,8 @@ import numpy as np
 import pytest
 
 from oracle import attention
-from oracle.dropout_fp64 import (attention_dropout, drop_threshold, keep_mask, philox4x32_10,
-                                 uniforms16)
+from oracle.dropout_fp64 import (attention_dropout, drop_threshold, keep_mask, keep_scale, philox4x32_10,
+                                 uniforms8)
 
 
 def _inputs(r, B, Hq, Hkv, Nq, Nkv, d):
@@ -31,14 +31,16 @@ def test_zero_probability_is_plain_attention():
 
 def test_threshold_quantisation():
     assert drop_threshold(0.0) == 0
-    assert drop_threshold(0.5) == 32768
-    assert drop_threshold(0.25) == 16384
-    assert drop_threshold(1.0 / 65536) == 1
-    assert drop_threshold(0.1) == 6554                 # 6553.6 rounds up
+    assert drop_threshold(0.5) == 128
+    assert drop_threshold(0.25) == 64
+    assert drop_threshold(1.0 / 256) == 1
+    assert drop_threshold(0.1) == 26                   # 25.6 rounds up
+    assert drop_threshold(0.001) == 0                  # below half a level: nothing is dropped
+    assert keep_scale(26) == 256 / 230
     with pytest.raises(ValueError):
         drop_threshold(1.0)
     with pytest.raises(ValueError):
-        drop_threshold(0.99999994)                     # below 1, but t would be 65536
+        drop_threshold(0.999)                          # below 1, but t would be 256
 
 
 def _bits(words):
@@ -54,8 +56,8 @@ def test_generator_bits_balanced_and_uniform():
     freq = bits.mean(axis=0)
     sigma = 0.5 / math.sqrt(n)
     assert np.all(np.abs(freq - 0.5) < 6 * sigma)
-    # top byte of each 16-bit half: 256 bins, chi-square with 255 degrees of freedom
-    u = np.concatenate([(out & 0xFFFF).ravel(), (out >> 16).ravel()]) >> 8
+    # every byte: 256 bins, chi-square with 255 degrees of freedom
+    u = np.concatenate([((out >> (8 * i)) & 0xFF).ravel() for i in range(4)])
     counts = np.bincount(u, minlength=256)
     e = len(u) / 256
     chi2 = float(((counts - e) ** 2 / e).sum())
@@ -89,7 +91,7 @@ def test_drop_rate_binomial():
         t = drop_threshold(p)
         keep = keep_mask(1, 3, np.arange(1000), 1000, seed=77, t=t)
         n = keep.size
-        q = t / 65536.0
+        q = t / 256.0
         dropped = n - int(keep.sum())
         assert abs(dropped - n * q) < 6 * math.sqrt(n * q * (1 - q))
 
@@ -100,10 +102,10 @@ def test_masks_depend_only_on_position():
     b = keep_mask(0, 2, np.arange(10, 50), 333, seed=9, t=t)
     assert np.array_equal(a[10:40], b[:30, :100])
     # distinct rows, heads, batches and seeds draw distinct bits
-    base = uniforms16(0, 0, [5], 256, seed=1)
-    for other in (uniforms16(0, 0, [6], 256, 1), uniforms16(0, 1, [5], 256, 1),
-                  uniforms16(1, 0, [5], 256, 1), uniforms16(0, 0, [5], 256, 2),
-                  uniforms16(0, 0, [5], 256, 1 << 32)):
+    base = uniforms8(0, 0, [5], 256, seed=1)
+    for other in (uniforms8(0, 0, [6], 256, 1), uniforms8(0, 1, [5], 256, 1),
+                  uniforms8(1, 0, [5], 256, 1), uniforms8(0, 0, [5], 256, 2),
+                  uniforms8(0, 0, [5], 256, 1 << 32)):
         assert not np.array_equal(base, other)
 
 
@@ -140,7 +142,7 @@ def test_scalar_evaluator(causal):
     q, k, v = _inputs(r, B, Hq, Hkv, Nq, Nkv, d)
     p_drop, seed, scale = 0.35, (7 << 32) | 99, 0.6
     o, _ = attention_dropout(q, k, v, causal, scale, p_drop, seed)
-    t = math.floor(float(np.float32(p_drop)) * 65536 + 0.5)
+    t = math.floor(float(np.float32(p_drop)) * 256 + 0.5)
     for h in range(Hq):
         for i in range(Nq):
             logits = {}
@@ -152,10 +154,10 @@ def test_scalar_evaluator(causal):
             den = sum(math.exp(s - mx) for s in logits.values())
             want = [0.0] * d
             for j, s in logits.items():
-                word = _philox_scalar([j // 8, i, h, 0], (seed & 0xFFFFFFFF, seed >> 32))[(j % 8) // 2]
-                u = (word >> 16) if j % 2 else (word & 0xFFFF)
+                word = _philox_scalar([j // 16, i, h, 0], (seed & 0xFFFFFFFF, seed >> 32))[(j % 16) // 4]
+                u = (word >> (8 * (j % 4))) & 0xFF
                 if u < t:
                     continue
                 for c in range(d):
-                    want[c] += math.exp(s - mx) / den * v[0, 0, j, c] * 65536 / (65536 - t)
+                    want[c] += math.exp(s - mx) / den * v[0, 0, j, c] * 256 / (256 - t)
             assert np.max(np.abs(o[0, h, i] - np.array(want))) < 1e-12
