@@ -290,42 +290,83 @@ def measure_device(wl, steps, warmup, world, stream, flush, inputs):
     return [s.elapsed_time(e) / 1e3 for s, e in ev]
 
 
-def measure_e2e(wl, steps, warmup, stream, host):
-    """Same metric with pinned host buffers: H2D inputs, attn_fwd, D2H O and LSE, per step."""
+E2E_SCHEDULE = "per step: H2D of its inputs, the call, D2H of its results; three streams, two device slots"
+
+
+def pipelined_steps(steps, warmup, copy_in, compute, copy_out, nbuf=2):
+    """Time `steps` end-to-end steps as a serving loop runs them: each step
+    copies its inputs from pinned host memory into device slot i % nbuf
+    (copy_in), runs the library call on that slot (compute) and copies its
+    results back to pinned host memory (copy_out), on three streams, so one
+    step's copies overlap its neighbours' compute.  Events keep a slot from
+    being refilled before its compute and its copy-out are done.  Returns the
+    seconds from the first copy in to the last copy out."""
     import torch
-    import blackwell_programming_gb300 as gb
+    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    in_done = [torch.cuda.Event() for _ in range(nbuf)]
+    c_done = [torch.cuda.Event() for _ in range(nbuf)]
+    out_done = [torch.cuda.Event() for _ in range(nbuf)]
+
+    def run(n):
+        for i in range(n):
+            b = i % nbuf
+            with torch.cuda.stream(s_in):
+                if i >= nbuf:
+                    s_in.wait_event(c_done[b])
+                copy_in(b)
+                in_done[b].record(s_in)
+            with torch.cuda.stream(s_c):
+                s_c.wait_event(in_done[b])
+                if i >= nbuf:
+                    s_c.wait_event(out_done[b])
+                compute(b, s_c)
+                c_done[b].record(s_c)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(c_done[b])
+                copy_out(b)
+                out_done[b].record(s_out)
+
+    run(warmup)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(s_in)
+    run(steps)
+    end.record(s_out)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def measure_e2e(wl, steps, warmup, stream, host):
+    """Same metric with pinned host buffers: per step H2D of Q, K, V, the
+    attention call, D2H of O and LSE (pipelined over steps, two slots)."""
+    import torch
     hq, hk, hv = host
-    dq = torch.empty_like(hq, device="cuda")
-    dk = torch.empty_like(hk, device="cuda")
-    dv = torch.empty_like(hv, device="cuda") if hv is not None else None
-    ho = torch.empty((wl.B, wl.Hq, wl.Nq, wl.d_v), dtype=o_torch_dtype()).pin_memory()
-    hl = torch.empty((wl.B, wl.Hq, wl.Nq), dtype=torch.float32).pin_memory()
-    o = torch.empty_like(ho, device="cuda")
-    lse = torch.empty_like(hl, device="cuda")
+    nb = 2
+    dq = [torch.empty_like(hq, device="cuda") for _ in range(nb)]
+    dk = [torch.empty_like(hk, device="cuda") for _ in range(nb)]
+    dv = [torch.empty_like(hv, device="cuda") for _ in range(nb)] if hv is not None else None
+    ho = [torch.empty((wl.B, wl.Hq, wl.Nq, wl.d_v), dtype=o_torch_dtype()).pin_memory() for _ in range(nb)]
+    hl = [torch.empty((wl.B, wl.Hq, wl.Nq), dtype=torch.float32).pin_memory() for _ in range(nb)]
+    o = [torch.empty_like(ho[0], device="cuda") for _ in range(nb)]
+    lse = [torch.empty_like(hl[0], device="cuda") for _ in range(nb)]
 
-    def step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
+    def copy_in(b):
+        dq[b].copy_(hq, non_blocking=True)
+        dk[b].copy_(hk, non_blocking=True)
         if dv is not None:
-            dv.copy_(hv, non_blocking=True)
-        v = dv if dv is not None else dk[..., : wl.d_v]
-        call_attn(dq, dk, v, wl, o, lse, stream)
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+            dv[b].copy_(hv, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            step()
-        torch.cuda.synchronize()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        for _ in range(steps):
-            step()
-        e.record(stream)
-        torch.cuda.synchronize()
-    secs = s.elapsed_time(e) / 1e3
+    def compute(b, s):
+        v = dv[b] if dv is not None else dk[b][..., : wl.d_v]
+        call_attn(dq[b], dk[b], v, wl, o[b], lse[b], s)
+
+    def copy_out(b):
+        ho[b].copy_(o[b], non_blocking=True)
+        hl[b].copy_(lse[b], non_blocking=True)
+
+    secs = pipelined_steps(steps, warmup, copy_in, compute, copy_out, nb)
     h2d = hq.numel() * 2 + hk.numel() * 2 + (hv.numel() * 2 if hv is not None else 0)
-    d2h = ho.numel() * 4 + hl.numel() * 4
+    d2h = ho[0].numel() * ho[0].element_size() + hl[0].numel() * 4
     return secs, h2d, d2h
 
 
@@ -371,7 +412,7 @@ def run_ours(args, wl):
         e2e_secs, h2d, d2h = measure_e2e(wl, args.steps, args.warmup, stream, (hq, hk, hv))
         e2e_max = reduce_max(e2e_secs, world)
         e2e = {"value": aggregate(flops * args.steps, e2e_max, world) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "schedule": E2E_SCHEDULE}
 
     peaks, peak_src = load_peaks()
     kind = ("decode" if wl.Nq == 1 else "latent_prefill") if wl.d_qk == 576 else "prefill"
@@ -514,26 +555,24 @@ def run_gemm_ours(args, gw):
 
     e2e = None
     if not args.no_e2e:
-        hc = torch.empty((gw.M, gw.N), dtype=torch.bfloat16).pin_memory()
-        da, db = torch.empty_like(a), torch.empty_like(b)
-        with torch.cuda.stream(stream):
-            def step():
-                da.copy_(ha, non_blocking=True)
-                db.copy_(hb, non_blocking=True)
-                gb.gemm_nt(da, db, out=c, stream=stream)
-                hc.copy_(c, non_blocking=True)
-            for _ in range(args.warmup):
-                step()
-            torch.cuda.synchronize()
-            s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s_ev.record(stream)
-            for _ in range(args.steps):
-                step()
-            e_ev.record(stream)
-            torch.cuda.synchronize()
-        e2e_max = reduce_max(s_ev.elapsed_time(e_ev) / 1e3, world)
+        hc = [torch.empty((gw.M, gw.N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        da = [torch.empty_like(a) for _ in range(2)]
+        db = [torch.empty_like(b) for _ in range(2)]
+        dc = [c, torch.empty_like(c)]
+
+        def copy_in(i):
+            da[i].copy_(ha, non_blocking=True)
+            db[i].copy_(hb, non_blocking=True)
+
+        def copy_out(i):
+            hc[i].copy_(dc[i], non_blocking=True)
+
+        secs = pipelined_steps(args.steps, args.warmup, copy_in,
+                               lambda i, s: gb.gemm_nt(da[i], db[i], out=dc[i], stream=s), copy_out)
+        e2e_max = reduce_max(secs, world)
         e2e = {"value": aggregate(gw.flops * args.steps, e2e_max, world) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": 2 * (gw.M + gw.N) * gw.K, "d2h_bytes_per_step": 2 * gw.M * gw.N}
+               "h2d_bytes_per_step": 2 * (gw.M + gw.N) * gw.K, "d2h_bytes_per_step": 2 * gw.M * gw.N,
+               "schedule": E2E_SCHEDULE}
 
     peaks, peak_src = load_peaks()
     per_launch = total / args.steps
@@ -709,28 +748,29 @@ def run_layer_ours(args, lw):
 
     e2e = None
     if not args.no_e2e:
-        hy = torch.empty((T, D), dtype=torch.bfloat16).pin_memory()
-        dx = torch.empty_like(x)
-        with torch.cuda.stream(stream):
-            def step():
-                dx.copy_(hx, non_blocking=True)
-                st = gb.attn_layer_raw(dx.data_ptr(), wq.data_ptr(), wo.data_ptr(), qkv.data_ptr(), o.data_ptr(),
-                                       y.data_ptr(), 0, B, N, D, Hq, Hkv, d, lw.causal, lw.scale, False, sp)
-                assert st == 0
-                hy.copy_(y, non_blocking=True)
-            for _ in range(args.warmup):
-                step()
-            torch.cuda.synchronize()
-            s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s_ev.record(stream)
-            for _ in range(args.steps):
-                step()
-            e_ev.record(stream)
-            torch.cuda.synchronize()
-        e2e_max = reduce_max(s_ev.elapsed_time(e_ev) / 1e3, world)
+        hy = [torch.empty((T, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        dx = [torch.empty_like(x) for _ in range(2)]
+        dqkv = [qkv, torch.empty_like(qkv)]
+        do_ = [o, torch.empty_like(o)]
+        dy = [y, torch.empty_like(y)]
+
+        def copy_in(i):
+            dx[i].copy_(hx, non_blocking=True)
+
+        def compute(i, s):
+            st = gb.attn_layer_raw(dx[i].data_ptr(), wq.data_ptr(), wo.data_ptr(), dqkv[i].data_ptr(),
+                                   do_[i].data_ptr(), dy[i].data_ptr(), 0, B, N, D, Hq, Hkv, d, lw.causal, lw.scale,
+                                   False, s.cuda_stream)
+            assert st == 0
+
+        def copy_out(i):
+            hy[i].copy_(dy[i], non_blocking=True)
+
+        secs = pipelined_steps(args.steps, args.warmup, copy_in, compute, copy_out)
+        e2e_max = reduce_max(secs, world)
         e2e = {"value": aggregate(lw.flops * args.steps, e2e_max, world) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": 2 * T * D, "d2h_bytes_per_step": 2 * T * D,
-               "api": "attn_layer_fwd (one call), weights resident"}
+               "api": "attn_layer_fwd (one call), weights resident", "schedule": E2E_SCHEDULE}
 
     # per-part FLOPs in the line's convention; the roofline is the slowest part's kernel
     att = 4.0 * B * Hq * N * N * d / (2.0 if lw.causal else 1.0)

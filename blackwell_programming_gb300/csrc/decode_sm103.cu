@@ -602,6 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // row.  `grid` is the decode kernel's grid size, which fixes where the
 // partials are.
 constexpr int kCombineWarps = 4;
+constexpr int kCombineMaxSlots = 4;   // partials per (half, sequence) handled in registers
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const DecodeParams p, int grid, float* o,
                                                                      uint16_t* o_bf16, float* lse) {
   __shared__ float tile[kCombineWarps][32][33];
@@ -633,40 +634,76 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Decod
     if (b1 <= b0) return -1;
     return static_cast<long long>(cta) * p.max_seg + (sg - b0 / tiles);
   };
-  float mx = -INFINITY;
-  for (int i = 0; i <= c_last - c_first; ++i) {
-    const long long s = slot_of(i);
-    if (s >= 0) mx = fmaxf(mx, p.lse_part[s * BM + rr]);
-  }
-  float tot = 0.f;
-  if (mx != -INFINITY) {
-    for (int i = 0; i <= c_last - c_first; ++i) {
-      const long long s = slot_of(i);
-      if (s < 0) continue;
-      const float ls = p.lse_part[s * BM + rr];
-      if (ls != -INFINITY) tot += expf(ls - mx);
-    }
-  }
-  const float inv = (tot > 0.f) ? 1.f / tot : 0.f;
-  const size_t out_rows = (static_cast<size_t>(plane) * p.group + r0) * (2 * DVH) + half * DVH;
+  const int ns = c_last - c_first + 1;
+  float mx = -INFINITY, tot = 0.f;
   float4 acc[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (mx != -INFINITY) {
-    for (int i = 0; i <= c_last - c_first; ++i) {
-      const long long s = slot_of(i);
-      if (s < 0) continue;
-      const float ls = p.lse_part[s * BM + rr];
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - mx) * inv;
-      const float4* src = reinterpret_cast<const float4*>(p.o_part) + (s * (DVH / 4) + blk * 8) * BM + rr;
+  if (ns <= kCombineMaxSlots) {
+    // Every slot's LSE in one round of loads, then every slot's 32 columns
+    // in one round, so the warp waits for memory twice, not once per slot.
+    long long sl[kCombineMaxSlots];
+    float ls[kCombineMaxSlots];
+#pragma unroll
+    for (int i = 0; i < kCombineMaxSlots; ++i) sl[i] = (i < ns) ? slot_of(i) : -1;
+#pragma unroll
+    for (int i = 0; i < kCombineMaxSlots; ++i) ls[i] = (sl[i] >= 0) ? p.lse_part[sl[i] * BM + rr] : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kCombineMaxSlots; ++i) mx = fmaxf(mx, ls[i]);
+    float4 x[kCombineMaxSlots][8];
+#pragma unroll
+    for (int i = 0; i < kCombineMaxSlots; ++i) {
+      const bool use = ls[i] != -INFINITY;   // also false for a missing slot
+      const float4* src = reinterpret_cast<const float4*>(p.o_part) + ((use ? sl[i] : 0) * (DVH / 4) + blk * 8) * BM + rr;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) x[i][c] = use ? src[static_cast<size_t>(c) * BM] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float w[kCombineMaxSlots];
+#pragma unroll
+    for (int i = 0; i < kCombineMaxSlots; ++i) {
+      w[i] = (ls[i] != -INFINITY) ? expf(ls[i] - mx) : 0.f;
+      tot += w[i];
+    }
+    const float inv = (tot > 0.f) ? 1.f / tot : 0.f;
+#pragma unroll
+    for (int i = 0; i < kCombineMaxSlots; ++i) {
+      const float wi = w[i] * inv;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        const float4 x = src[static_cast<size_t>(c) * BM];
-        acc[c].x += w * x.x; acc[c].y += w * x.y; acc[c].z += w * x.z; acc[c].w += w * x.w;
+        acc[c].x += wi * x[i][c].x; acc[c].y += wi * x[i][c].y; acc[c].z += wi * x[i][c].z; acc[c].w += wi * x[i][c].w;
+      }
+    }
+  } else {
+    for (int i = 0; i < ns; ++i) {
+      const long long s = slot_of(i);
+      if (s >= 0) mx = fmaxf(mx, p.lse_part[s * BM + rr]);
+    }
+    if (mx != -INFINITY) {
+      for (int i = 0; i < ns; ++i) {
+        const long long s = slot_of(i);
+        if (s < 0) continue;
+        const float ls = p.lse_part[s * BM + rr];
+        if (ls != -INFINITY) tot += expf(ls - mx);
+      }
+    }
+    const float inv = (tot > 0.f) ? 1.f / tot : 0.f;
+    if (mx != -INFINITY) {
+      for (int i = 0; i < ns; ++i) {
+        const long long s = slot_of(i);
+        if (s < 0) continue;
+        const float ls = p.lse_part[s * BM + rr];
+        if (ls == -INFINITY) continue;
+        const float w = expf(ls - mx) * inv;
+        const float4* src = reinterpret_cast<const float4*>(p.o_part) + (s * (DVH / 4) + blk * 8) * BM + rr;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float4 x = src[static_cast<size_t>(c) * BM];
+          acc[c].x += w * x.x; acc[c].y += w * x.y; acc[c].z += w * x.z; acc[c].w += w * x.w;
+        }
       }
     }
   }
+  const size_t out_rows = (static_cast<size_t>(plane) * p.group + r0) * (2 * DVH) + half * DVH;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     tile[wib][lane][4 * c] = acc[c].x;

@@ -57,6 +57,10 @@ SMALL = [
       scale=1 / math.sqrt(192), v_aliases_k=True),
     W("decode_two_kv_heads", B=3, Hq=64, Hkv=2, Nq=1, Nkv=1111, d_qk=576, d_v=512, causal=True,
       scale=1 / math.sqrt(192), v_aliases_k=True),
+    # many short sequences: each output row merges two to four split partials
+    # (the combine's in-register path; the cases above merge more)
+    W("decode_many_sequences", B=32, Hq=16, Hkv=1, Nq=1, Nkv=640, d_qk=576, d_v=512, causal=False,
+      scale=1 / math.sqrt(192), v_aliases_k=True),
     # one long sequence: every output row merges more than 32 split partials
     W("decode_one_long_sequence", B=1, Hq=16, Hkv=1, Nq=1, Nkv=100000, d_qk=576, d_v=512, causal=False,
       scale=1 / math.sqrt(192), v_aliases_k=True),
