@@ -291,6 +291,7 @@ def measure_device(wl, steps, warmup, world, stream, flush, inputs):
 
 
 E2E_SCHEDULE = "per step: H2D of its inputs, the call, D2H of its results; three streams, two device slots"
+E2E_SERIAL = False
 
 
 def pipelined_steps(steps, warmup, copy_in, compute, copy_out, nbuf=2):
@@ -302,7 +303,12 @@ def pipelined_steps(steps, warmup, copy_in, compute, copy_out, nbuf=2):
     being refilled before its compute and its copy-out are done.  Returns the
     seconds from the first copy in to the last copy out."""
     import torch
-    s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    if E2E_SERIAL:
+        # one stream: each step's copies and call run back to back
+        nbuf = 1
+        s_in = s_c = s_out = torch.cuda.Stream()
+    else:
+        s_in, s_c, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     in_done = [torch.cuda.Event() for _ in range(nbuf)]
     c_done = [torch.cuda.Event() for _ in range(nbuf)]
     out_done = [torch.cuda.Event() for _ in range(nbuf)]
@@ -815,10 +821,15 @@ def main(argv=None):
     ap.add_argument("--heads", type=int, default=None, help="override the workload's query heads (profiling cases)")
     ap.add_argument("--out", default="fp32", choices=["fp32", "bf16"], help="O output type (fp32 is the measured configuration)")
     ap.add_argument("--dropout", type=float, default=0.0, help="dropout probability on the softmax weights (prefill shapes)")
+    ap.add_argument("--e2e-schedule", default="pipelined", choices=["pipelined", "serial"],
+                    help="e2e steps overlapped on three streams (default) or back to back on one")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)      # at least three untimed warm-up steps
-    global O_DTYPE, DROPOUT
+    global O_DTYPE, DROPOUT, E2E_SERIAL, E2E_SCHEDULE
     O_DTYPE = args.out
+    if args.e2e_schedule == "serial":
+        E2E_SERIAL = True
+        E2E_SCHEDULE = "per step: H2D of its inputs, the call, D2H of its results; one stream, back to back"
     DROPOUT = args.dropout
     if DROPOUT > 0.0 and O_DTYPE != "fp32":
         ap.error("--dropout writes fp32 O")
