@@ -34,7 +34,10 @@ Pinned by tests/test_oracle_dropout.py: p = 0 is plain attention, the
 generator's output bits are balanced and every input bit avalanches, the drop
 rate and the expectation of O match their targets within binomial and
 central-limit bounds, masks do not depend on the problem's size, and a
-scalar pure-Python evaluator agrees.
+scalar pure-Python evaluator agrees.  Parity unpinned for the exact bit
+stream: the generator's constants and round count follow the published
+definition, but the reference implementation's known-answer vectors are not
+reproduced here, so only the properties above fix the bits.
 """
 from __future__ import annotations
 
