@@ -63,8 +63,8 @@ struct Cfg {
   static constexpr uint32_t KV_BYTES = BN * D * 2;
   static constexpr uint32_t CHUNK_Q = BM * 128;      // one 64-column chunk of a Q tile
   static constexpr uint32_t CHUNK_KV = BN * 128;
-  static constexpr int KS = (D == 128) ? 3 : 4;      // K stages
-  static constexpr int VS = (D == 128) ? 2 : 4;      // V stages
+  static constexpr int KS = (D == 128) ? 2 : 4;      // K stages
+  static constexpr int VS = (D == 128) ? 3 : 4;      // V stages
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + KS * KV_BYTES;
