@@ -436,7 +436,8 @@ def run_ours(args, wl):
                 "kernel": "latent_kernel (decode mode) + combine_kernel (one step)",
                 "algorithmic_bytes_per_launch": algorithmic_bytes(wl),
                 "tensor_tflops": flops / per_launch / 1e12}
-    roof["traffic"] = committed_traffic(kind, wl.name) if O_DTYPE == "fp32" and DROPOUT == 0.0 else None
+    traffic_key = wl.name + ("_dropout%g" % DROPOUT if DROPOUT > 0.0 else "")
+    roof["traffic"] = committed_traffic(kind, traffic_key) if O_DTYPE == "fp32" else None
     launches = (2 if kind == "decode" else 1) * args.steps
 
     if rank == 0:
