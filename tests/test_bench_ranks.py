@@ -64,3 +64,22 @@ def test_reference_arm_prints_on_rank_zero_only(tmp_path):
     assert r.returncode == 0
     line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+@pytest.mark.parametrize("workload", ["gemm_qkv_proj", "layer_gqa_d128", "causal_d64_bigq"])
+def test_reference_arm_line_contract(workload):
+    """The reference arm's JSON line carries the keys the benchmark contract
+    names, for the attention, GEMM and layer workloads."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", workload,
+                        "--steps", "1", "--warmup", "1", "--ref-budget", "0.3"],
+                       capture_output=True, text=True, env=env, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "TFLOP/s"
+    assert line["config"]["workload"] == workload
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
