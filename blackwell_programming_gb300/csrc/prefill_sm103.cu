@@ -124,6 +124,36 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
   return __all_sync(kFull, ok);
 }
 
+// Dropout keep flags.  Key 4m + k of a generator word w is kept iff its byte
+// u_k = byte k of w satisfies u_k >= t, i.e. iff u_k + (256 - t) reaches 256.
+// Each 16-bit lane takes one byte shifted up by 7 (the even bytes, then the
+// odd ones), so with cdrop = (256 - t) * (2^7 + 2^23) that carry lands on bit
+// 15 or 31 and no lane overflows into the next (u + 256 - t < 512).  One byte
+// permute then gathers the four carries into the top bits of the result's
+// bytes: byte 0 <- key 1, byte 1 <- key 0, byte 2 <- key 3, byte 3 <- key 2.
+__device__ __forceinline__ uint32_t keep_flags(uint32_t w, uint32_t cdrop) {
+  uint32_t wo, f;
+  asm("prmt.b32 %0, %1, 0, 0x4341;" : "=r"(wo) : "r"(w));   // bytes 1 and 3 down to 0 and 2
+  const uint32_t ev = (w & 0x00FF00FFu) * 128u + cdrop;
+  const uint32_t od = wo * 128u + cdrop;
+  asm("prmt.b32 %0, %1, %2, 0x3715;" : "=r"(f) : "r"(ev), "r"(od));
+  return f;
+}
+
+// Two flag words in one register: fa's flags stay on bit 7 of each byte,
+// fb's move to bit 6 (the other bits are don't-care).
+__device__ __forceinline__ uint32_t keep_flags2(uint32_t fa, uint32_t fb) {
+  return (fa & 0x80808080u) | ((fb >> 1) & 0x40404040u);
+}
+
+// AND masks for the two bf16 pairs of a flag word's keys (m01: keys 0 and 1
+// in the low and high half; m23: keys 2 and 3): a sign-replicating byte
+// permute spreads each flag bit over the 16 bits of its key's half.
+__device__ __forceinline__ void keep_pair_masks(uint32_t f, uint32_t& m01, uint32_t& m23) {
+  asm("prmt.b32 %0, %1, 0, 0x8899;" : "=r"(m01) : "r"(f));
+  asm("prmt.b32 %0, %1, 0, 0xAABB;" : "=r"(m23) : "r"(f));
+}
+
 template <int D, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -372,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tm + lane_addr + C::col_s(t);
     const uint32_t tO = tm + lane_addr + C::col_o(t);
     const float sl2 = p.scale_log2;
+    const uint32_t cdrop = (256u - p.drop_t) * 0x00800080u;
     const int delta = p.Nkv - p.Nq;
     uint32_t sph = 0, ofph = 0;
     for (int it = 0;; ++it) {
@@ -384,35 +415,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
-        // Dropout keep bits of this row's 128 keys (bit c of keep[w] is key
-        // 32 w + c), drawn while the tensor core computes S: one generator
-        // call per 16 keys, one byte per key.  A byte u is kept iff
-        // u >= t, i.e. iff u + (256 - t) carries into bit 8: two bytes at a
-        // time in 16-bit lanes that cannot overflow.
-        uint32_t keep[4] = {0u, 0u, 0u, 0u};
+        // Dropout: the keep flags of this row's 128 keys, drawn while the
+        // tensor core computes S (one generator call per 16 keys), so the
+        // exp loop after the S wait only expands them into pair masks.
+        uint32_t rw[DROP ? BN / 8 : 1];
         if constexpr (DROP) {
-          const uint32_t c2 = (256u - p.drop_t) * 0x00010001u;
-#pragma unroll 1
+#pragma unroll
           for (int g = 0; g < BN / 16; ++g) {
             const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j * (BN / 16) + g),
                                                      static_cast<uint32_t>(row), static_cast<uint32_t>(U.h),
                                                      static_cast<uint32_t>(U.b)),
                                           p.seed_lo, p.seed_hi);
-            const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
-            uint32_t bits = 0u;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint32_t ev = (w4[q] & 0x00FF00FFu) + c2;          // bytes 0 and 2
-              const uint32_t od = ((w4[q] >> 8) & 0x00FF00FFu) + c2;   // bytes 1 and 3
-              const uint32_t nib = ((ev >> 8) & 1u) | ((od >> 7) & 2u) | ((ev >> 22) & 4u) | ((od >> 21) & 8u);
-              bits |= nib << (4 * q);
-            }
-            const uint32_t sh = bits << (16 * (g & 1));
-            const int wsel = g >> 1;
-            keep[0] |= wsel == 0 ? sh : 0u;
-            keep[1] |= wsel == 1 ? sh : 0u;
-            keep[2] |= wsel == 2 ? sh : 0u;
-            keep[3] |= wsel == 3 ? sh : 0u;
+            // two words' flags per register: the first word's on bit 7 of
+            // each byte, the second's on bit 6
+            rw[2 * g] = keep_flags2(keep_flags(r.x, cdrop), keep_flags(r.y, cdrop));
+            rw[2 * g + 1] = keep_flags2(keep_flags(r.z, cdrop), keep_flags(r.w, cdrop));
           }
         }
         if (!(ok = warp_wait(bar(C::B_SFULL + t), sph, wctx))) break;
@@ -481,16 +498,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < BN / 4; ++i) {
             const int e = h * (BN / 4) + i;
             const uint64_t x = f2_fma(f2_pack(v[2 * e], v[2 * e + 1]), c2, nb2);
-            float p0 = ex2(f2_lo(x));
-            float p1 = ex2(f2_hi(x));
+            const float p0 = ex2(f2_lo(x));
+            const float p1 = ex2(f2_hi(x));
             acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-            if constexpr (DROP) {
-              // dropout after the row sum: the normaliser counts every key,
-              // P V sees only the kept ones
-              if (!((keep[(2 * e) >> 5] >> ((2 * e) & 31)) & 1u)) p0 = 0.f;
-              if (!((keep[(2 * e + 1) >> 5] >> ((2 * e + 1) & 31)) & 1u)) p1 = 0.f;
-            }
             pk[i] = pack_bf16x2(p0, p1);
+          }
+          if constexpr (DROP) {
+            // dropout after the row sum: the normaliser counts every key,
+            // P V sees only the kept ones
+#pragma unroll
+            for (int q = 0; q < BN / 16; ++q) {
+              const uint32_t fa = rw[h * (BN / 16) + q];
+              uint32_t m01, m23;
+              keep_pair_masks(fa, m01, m23);
+              pk[4 * q] &= m01;
+              pk[4 * q + 1] &= m23;
+              keep_pair_masks(fa << 1, m01, m23);
+              pk[4 * q + 2] &= m01;
+              pk[4 * q + 3] &= m23;
+            }
           }
           tmem_st32u(tS + h * (BN / 4), pk);
           tmem_st_wait();
