@@ -34,10 +34,14 @@ Pinned by tests/test_oracle_dropout.py: p = 0 is plain attention, the
 generator's output bits are balanced and every input bit avalanches, the drop
 rate and the expectation of O match their targets within binomial and
 central-limit bounds, masks do not depend on the problem's size, and a
-scalar pure-Python evaluator agrees.  Parity unpinned for the exact bit
-stream: the generator's constants and round count follow the published
-definition, but the reference implementation's known-answer vectors are not
-reproduced here, so only the properties above fix the bits.
+scalar pure-Python evaluator agrees.  The key schedule's Weyl constants equal
+their closed forms (the golden ratio's fractional part and sqrt(3) - 1 in
+32-bit fixed point), and an inverse written from the round definition
+recovers every counter, which fixes the round structure, the word order and
+the round count.  Parity unpinned for the two round multipliers' values: they
+follow the published definition, but the reference implementation's
+known-answer vectors are not reproduced here, so only the statistical
+properties above and their oddness fix them.
 """
 from __future__ import annotations
 

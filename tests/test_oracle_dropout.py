@@ -161,3 +161,50 @@ def test_scalar_evaluator(causal):
                 for c in range(d):
                     want[c] += math.exp(s - mx) / den * v[0, 0, j, c] * 256 / (256 - t)
             assert np.max(np.abs(o[0, h, i] - np.array(want))) < 1e-12
+
+
+def test_weyl_constants_closed_form():
+    """The key schedule's increments are the published Weyl constants: the
+    golden ratio's fractional part and sqrt(3) - 1, in 32-bit fixed point
+    (exact integer square roots, no floating point)."""
+    from oracle import dropout_fp64 as dr
+    assert dr.PHILOX_W0 == (math.isqrt(5 << 64) - (1 << 32)) // 2
+    assert dr.PHILOX_W1 == math.isqrt(3 << 64) - (1 << 32)
+    # the round multipliers must be odd, or the round would not be a bijection
+    assert dr.PHILOX_M0 & 1 and dr.PHILOX_M1 & 1
+
+
+def _philox_inverse(out, key, m0, m1, w0, w1, rounds=10):
+    """Undo the rounds from the last one back: lo(M * x) gives x through the
+    inverse of the odd multiplier modulo 2^32, hi(M * x) then unmasks the
+    word that was XORed with it."""
+    m0i, m1i = pow(m0, -1, 1 << 32), pow(m1, -1, 1 << 32)
+    keys = [((key[0] + r * w0) & 0xFFFFFFFF, (key[1] + r * w1) & 0xFFFFFFFF) for r in range(rounds)]
+    y0, y1, y2, y3 = out
+    for k0, k1 in reversed(keys):
+        x2 = (y1 * m1i) & 0xFFFFFFFF
+        x0 = (y3 * m0i) & 0xFFFFFFFF
+        x1 = y0 ^ ((m1 * x2) >> 32) ^ k0
+        x3 = y2 ^ ((m0 * x0) >> 32) ^ k1
+        y0, y1, y2, y3 = x0, x1, x2, x3
+    return [y0, y1, y2, y3]
+
+
+def test_rounds_invert_to_the_counter():
+    """Each round is a bijection of the counter for a fixed key.  An inverse
+    written from the round's definition must recover every counter from the
+    oracle's output: a swapped output word, a hi/lo mix-up, a wrong round
+    count or a key schedule that advances before the first round all break
+    the round trip."""
+    from oracle import dropout_fp64 as dr
+    r = np.random.default_rng(11)
+    ctr = r.integers(0, 1 << 32, size=(64, 4), dtype=np.uint64)
+    key = (0x0BADC0DE, 0xFEEDFACE)
+    out = philox4x32_10(ctr, key)
+    for c, o in zip(ctr.tolist(), out.tolist()):
+        back = _philox_inverse(o, key, dr.PHILOX_M0, dr.PHILOX_M1, dr.PHILOX_W0, dr.PHILOX_W1)
+        assert back == c
+    # nine or eleven rounds do not invert it
+    o = out[0].tolist()
+    for rounds in (9, 11):
+        assert _philox_inverse(o, key, dr.PHILOX_M0, dr.PHILOX_M1, dr.PHILOX_W0, dr.PHILOX_W1, rounds) != ctr[0].tolist()
