@@ -38,10 +38,9 @@ scalar pure-Python evaluator agrees.  The key schedule's Weyl constants equal
 their closed forms (the golden ratio's fractional part and sqrt(3) - 1 in
 32-bit fixed point), and an inverse written from the round definition
 recovers every counter, which fixes the round structure, the word order and
-the round count.  Parity unpinned for the two round multipliers' values: they
-follow the published definition, but the reference implementation's
-known-answer vectors are not reproduced here, so only the statistical
-properties above and their oddness fix them.
+the round count.  The published known-answer vectors of Philox4x32-10 (the
+Random123 library's, tests/golden/philox4x32_10_kat.json) fix the two round
+multipliers and the whole output.
 """
 from __future__ import annotations
 
