@@ -144,7 +144,8 @@ def attn_fwd_dropout(q, k, v, p_drop: float, seed: int, causal: bool = False, sc
     """Attention with dropout on the softmax weights (attn_fwd_dropout in gbattn.h).
 
     q: bf16 [B, Hq, Nq, d]; k, v: bf16 [B, Hkv, Nkv, d]; d 64 or 128, all
-    contiguous.  p_drop in [0, 1); seed: 64-bit integer.  Returns (o fp32
+    contiguous.  p_drop = 0 or in [1/512, 1) (a nonzero p below 1/512 would
+    round to no dropout and is refused); seed: 64-bit integer.  Returns (o fp32
     [B, Hq, Nq, d], lse fp32 [B, Hq, Nq] or None).
     """
     import torch

@@ -48,7 +48,8 @@ struct DeviceInfo {
   int status = ATTN_OK;
   int num_sms = 0;
   unsigned* err = nullptr;
-  // Stream-ordered pool for the split-KV workspace.  Its release threshold
+  // Stream-ordered pool for the split-KV workspace, created by decode_pool()
+  // on the first decode call that needs it.  Its release threshold
   // is unlimited, so memory freed at the end of one call is reused by the
   // next instead of being unmapped at every synchronisation and mapped again
   // (which the default pool does, at about 0.1 ms per call for a 40 MB
@@ -83,15 +84,6 @@ int device_info(DeviceInfo** out) {
     void* p = nullptr;
     if ((e = cudaGetSymbolAddress(&p, g_device_error)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
     d.err = static_cast<unsigned*>(p);
-    cudaMemPoolProps props;
-    std::memset(&props, 0, sizeof(props));
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    if ((e = cudaMemPoolCreate(&d.pool, &props)) != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
-    uint64_t keep = UINT64_MAX;
-    if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
-      return cuda_fail(e, "cudaMemPoolSetAttribute");
     if (g_encode == nullptr) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -103,6 +95,32 @@ int device_info(DeviceInfo** out) {
     d.ready = true;
   }
   *out = &d;
+  return ATTN_OK;
+}
+
+// The decode workspace pool of the current device, created on first use (only
+// attn_fwd's split-KV decode takes workspace from it).
+int decode_pool(DeviceInfo* d, cudaMemPool_t* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (d->pool == nullptr) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+    uint64_t keep = UINT64_MAX;
+    if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return cuda_fail(e, "cudaMemPoolSetAttribute");
+    }
+    d->pool = pool;
+  }
+  *out = d->pool;
   return ATTN_OK;
 }
 
@@ -384,8 +402,10 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint1
     const int grid = static_cast<int>(std::min<long long>(total, dev->num_sms));
     p.max_seg = decode_max_segments(planes, p.tiles, grid);
     const size_t n_slots = static_cast<size_t>(grid) * p.max_seg * 128;
+    cudaMemPool_t pool = nullptr;
+    if ((st = decode_pool(dev, &pool)) != ATTN_OK) return st;
     void* ws = nullptr;
-    if ((e = cudaMallocFromPoolAsync(&ws, n_slots * (256 + 1) * sizeof(float), dev->pool, stream)) != cudaSuccess)
+    if ((e = cudaMallocFromPoolAsync(&ws, n_slots * (256 + 1) * sizeof(float), pool, stream)) != cudaSuccess)
       return cuda_fail(e, "cudaMallocFromPoolAsync(decode workspace)");
     p.o_part = static_cast<float*>(ws);
     p.lse_part = p.o_part + n_slots * 256;
@@ -463,6 +483,11 @@ int attn_fwd_dropout(const void* q, const void* k, const void* v, float* o, floa
   if (!(p_drop >= 0.f && p_drop < 1.f)) return ATTN_ERR_INVALID_ARG;   // also refuses NaN
   const double tf = std::floor(static_cast<double>(p_drop) * 256.0 + 0.5);
   if (tf >= 256.0) return ATTN_ERR_INVALID_ARG;                         // would drop every weight
+  if (p_drop > 0.f && tf == 0.0) {
+    std::snprintf(t_cuda_error, sizeof(t_cuda_error),
+                  "p_drop %g is below the 8-bit resolution (1/512) and would drop nothing", p_drop);
+    return ATTN_ERR_INVALID_ARG;
+  }
   const Dropout drop{static_cast<uint32_t>(tf), seed};
   return attn_fwd_impl(q, k, v, o, nullptr, lse, B, Hq, Hkv, Nq, Nkv, d_qk, d_v, causal, scale, stream, drop);
 }
@@ -505,6 +530,7 @@ int attn_fwd_bshd(const void* q, const void* k, const void* v, void* o, float* l
 int attn_layer_fwd(const void* x, const void* w_qkv, const void* w_o, void* qkv, void* o, void* y, float* lse, int B,
                    int N, int d_model, int Hq, int Hkv, int d, int causal, float scale, int y_fp32,
                    attn_stream_t stream) {
+  t_cuda_error[0] = '\0';
   if (x == nullptr || w_qkv == nullptr || w_o == nullptr || qkv == nullptr || o == nullptr || y == nullptr)
     return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || N <= 0 || d_model <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0)

@@ -79,7 +79,8 @@ typedef enum {
  * blocks of 128 query rows, which writes O and LSE directly.  The decode
  * path takes a
  * stream-ordered workspace (cudaMallocFromPoolAsync / cudaFreeAsync on
- * `stream`) from a memory pool the library creates per device; the pool
+ * `stream`) from a memory pool the library creates per device on the first
+ * decode call; the pool
  * keeps freed memory for the next call (it never shrinks below the largest
  * workspace used so far), so repeated calls map no new memory.
  *
@@ -123,9 +124,10 @@ int attn_fwd_bf16out(const void* q, const void* k, const void* v, void* o, float
  *
  * Arguments, layouts and errors as attn_fwd, O fp32, for the prefill shapes
  * (d_qk == d_v, 64 or 128); ATTN_ERR_UNSUPPORTED for the latent shape and
- * ATTN_ERR_INVALID_ARG unless 0 <= p_drop and t < 256.  p_drop == 0 (or any
- * p_drop < 1/512, which rounds to t = 0) runs
- * the same kernel as attn_fwd.
+ * ATTN_ERR_INVALID_ARG unless p_drop == 0 or 1/512 <= p_drop with t < 256:
+ * a nonzero p_drop below 1/512 would round to t = 0 and silently drop
+ * nothing, so it is refused rather than run.  p_drop == 0 runs the same
+ * kernel as attn_fwd.
  */
 int attn_fwd_dropout(const void* q, const void* k, const void* v, float* o, float* lse,
                      int B, int Hq, int Hkv, int Nq, int Nkv, int d_qk, int d_v,
@@ -199,8 +201,9 @@ size_t attn_decode_workspace_bytes(int B, int Hkv, int Nkv);
  * GPU's free memory, a serving loop with a fixed memory budget that must not
  * fail in the middle of a request, or a plug-in whose host forbids
  * allocation.  attn_fwd takes its decode workspace from a stream-ordered
- * pool (cudaMallocFromPoolAsync);
- * this entry point calls no cudaMalloc, cudaFree or any allocating routine.
+ * pool (cudaMallocFromPoolAsync), which it creates on its first decode call
+ * on a device; this entry point neither creates nor uses that pool, and
+ * calls no cudaMalloc, cudaFree or any allocating routine.
  *
  * Its split partials go to one static device array of 48 MiB declared in
  * the library.  Every GPU that loads the library holds that array until the

@@ -123,10 +123,17 @@ def _dropout_raw(lib, p_drop, d_qk=128, d_v=128, v_ptr=P * 3):
                                 ctypes.c_float(0.1), ctypes.c_float(p_drop), ctypes.c_ulonglong(7), None)
 
 
-@pytest.mark.parametrize("p_drop", [1.0, -0.1, float("nan"), 0.999, 2.0])
+@pytest.mark.parametrize("p_drop", [1.0, -0.1, float("nan"), 0.999, 2.0, 1e-3, 1.0 / 1024, 1e-30])
 def test_dropout_probability_checked(lib, p_drop):
-    # 0.999 is below 1 but rounds to t = 256, which would drop every weight
+    # 0.999 is below 1 but rounds to t = 256, which would drop every weight;
+    # a nonzero p below 1/512 rounds to t = 0 and would silently drop nothing
     assert _dropout_raw(lib, p_drop) == gb.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("p_drop", [0.0, 1.0 / 512, 0.1, 0.99])
+def test_dropout_probability_accepted(lib, p_drop):
+    # past the argument checks (without a GPU the call then fails on the device)
+    assert _dropout_raw(lib, p_drop) != gb.ATTN_ERR_INVALID_ARG
 
 
 def test_dropout_latent_shape_unsupported(lib):

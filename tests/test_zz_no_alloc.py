@@ -76,3 +76,30 @@ def test_noalloc_rejects_problems_beyond_the_static_scratch(gb):
     assert "static array" in gb.attn_last_cuda_error()
     torch.cuda.synchronize()
     assert torch.count_nonzero(o) == 0
+
+
+def test_noalloc_reserves_no_device_memory(gb):
+    # The property the entry point exists for: once the library is loaded on
+    # the device (the first call), further calls take no device memory.  All
+    # buffers are made before the measurement, so the only thing that could
+    # move the device's free memory is the library itself.
+    B, Hq, Hkv, Nkv = 16, 128, 1, 4096
+    wl = syn.Workload("noalloc_mem", B, Hq, Hkv, 1, Nkv, 576, 512, False, 1 / math.sqrt(192), v_aliases_k=True)
+    q, k, _ = to_torch(syn.make_inputs(wl))
+    o = torch.empty((B, Hq, 1, 512), device="cuda")
+    lse = torch.empty((B, Hq, 1), device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        st = gb.attn_decode_fwd_noalloc(q.data_ptr(), k.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                        B, Hq, Hkv, Nkv, wl.scale, stream)
+        assert st == gb.ATTN_OK, (gb.attn_status_string(st), gb.attn_last_cuda_error())
+
+    call()
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert gb.attn_check_device(reset=True) == 0
