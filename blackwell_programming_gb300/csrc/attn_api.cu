@@ -181,6 +181,24 @@ int make_prefill_map(CUtensorMap* m, const void* base, int B, int H, int N, int 
   return make_map4(m, base, dims, st, 1, 128);
 }
 
+// The latent kernel's maps: Q [q_planes, q_rows, 576] and K [k_planes,
+// k_rows, 576] bf16, each seen as (64 features, rows, 9 chunks, planes) with
+// the 128-byte chunk stride inside the 1152-byte row stride, so that one box
+// of r rows x c chunks is c consecutive chunk images of r rows.
+int make_latent_maps(LatentMaps* m, const void* q, uint64_t q_rows, uint64_t q_planes, const void* k, uint64_t k_rows,
+                     uint64_t k_planes) {
+  const uint64_t row = 576 * 2;
+  const uint64_t qd[4] = {64, q_rows, 9, q_planes};
+  const uint64_t qs[3] = {row, 128, row * q_rows};
+  const uint64_t kd[4] = {64, k_rows, 9, k_planes};
+  const uint64_t ks[3] = {row, 128, row * k_rows};
+  int st;
+  if ((st = make_map4(&m->q, q, qd, qs, kLatentQRows, kLatentQChunks)) != ATTN_OK) return st;
+  if ((st = make_map4(&m->k5, k, kd, ks, kLatentKeyRows, 5)) != ATTN_OK) return st;
+  if ((st = make_map4(&m->k4, k, kd, ks, kLatentKeyRows, 4)) != ATTN_OK) return st;
+  return make_map4(&m->k1, k, kd, ks, kLatentKeyRows, 1);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool env_flag(const char* name) {
@@ -360,10 +378,9 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint1
       return st;
   } else if (!decode) {
     // latent shape, Nq > 1: the decode kernel in prefill mode
-    CUtensorMap tq, tk;
-    const uint64_t rs = static_cast<uint64_t>(d_qk) * 2;
-    if ((st = make_map(&tq, q, d_qk, Nq, static_cast<uint64_t>(B) * Hq, rs, rs * Nq, 128)) != ATTN_OK) return st;
-    if ((st = make_map(&tk, k, d_qk, Nkv, static_cast<uint64_t>(B) * Hkv, rs, rs * Nkv, decode_key_tile())) != ATTN_OK)
+    LatentMaps maps;
+    if ((st = make_latent_maps(&maps, q, Nq, static_cast<uint64_t>(B) * Hq, k, Nkv, static_cast<uint64_t>(B) * Hkv)) !=
+        ATTN_OK)
       return st;
     LatentPrefillParams p{};
     p.q = static_cast<const uint16_t*>(q);
@@ -381,15 +398,13 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint1
     p.num_units = 2 * B * Hq * p.nqb;
     p.scale_log2 = scale_log2;
     p.err = dev->err;
-    if ((e = launch_latent_prefill(tq, tk, p, dev->num_sms, stream)) != cudaSuccess)
+    if ((e = launch_latent_prefill(maps, p, dev->num_sms, stream)) != cudaSuccess)
       return cuda_fail(e, "latent prefill launch");
   } else {
     const int group = Hq / Hkv;
     const int planes = B * Hkv;
-    CUtensorMap tq, tk;
-    const uint64_t rs = static_cast<uint64_t>(d_qk) * 2;
-    if ((st = make_map(&tq, q, d_qk, group, planes, rs, rs * group, 128)) != ATTN_OK) return st;
-    if ((st = make_map(&tk, k, d_qk, Nkv, planes, rs, rs * Nkv, decode_key_tile())) != ATTN_OK) return st;
+    LatentMaps maps;
+    if ((st = make_latent_maps(&maps, q, group, planes, k, Nkv, planes)) != ATTN_OK) return st;
     DecodeParams p{};
     p.q = static_cast<const uint16_t*>(q);
     p.planes = planes;
@@ -409,7 +424,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint1
       return cuda_fail(e, "cudaMallocFromPoolAsync(decode workspace)");
     p.o_part = static_cast<float*>(ws);
     p.lse_part = p.o_part + n_slots * 256;
-    if ((e = launch_decode(tq, tk, p, grid, stream)) != cudaSuccess) {
+    if ((e = launch_decode(maps, p, grid, stream)) != cudaSuccess) {
       cudaFreeAsync(ws, stream);
       return cuda_fail(e, "decode launch");
     }
@@ -612,7 +627,6 @@ extern "C" int attn_decode_fwd_noalloc(const void* q, const void* kv, float* o, 
   float* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != ATTN_OK) return st;
 
-  const int d_qk = 576;
   const int group = Hq / Hkv;
   const int planes = B * Hkv;
   DecodeParams p{};
@@ -633,16 +647,14 @@ extern "C" int attn_decode_fwd_noalloc(const void* q, const void* kv, float* o, 
                   kNoAllocScratchBytes);
     return ATTN_ERR_SCRATCH_LIMIT;
   }
-  CUtensorMap tq, tk;
-  const uint64_t rs = static_cast<uint64_t>(d_qk) * 2;
-  if ((st = make_map(&tq, q, d_qk, group, planes, rs, rs * group, 128)) != ATTN_OK) return st;
-  if ((st = make_map(&tk, kv, d_qk, Nkv, planes, rs, rs * Nkv, decode_key_tile())) != ATTN_OK) return st;
+  LatentMaps maps;
+  if ((st = make_latent_maps(&maps, q, group, planes, kv, Nkv, planes)) != ATTN_OK) return st;
   // Every slot the combine kernel reads is written first by the decode
   // kernel in the same call, so nothing needs clearing between calls.
   p.o_part = scratch;
   p.lse_part = scratch + n_slots * 256;
   cudaError_t e;
-  if ((e = launch_decode(tq, tk, p, grid, stream)) != cudaSuccess) return cuda_fail(e, "decode launch");
+  if ((e = launch_decode(maps, p, grid, stream)) != cudaSuccess) return cuda_fail(e, "decode launch");
   if ((e = launch_combine(p, grid, o, nullptr, lse, stream)) != cudaSuccess) return cuda_fail(e, "combine launch");
   if (check_env()) return read_device_error(stream, dev->err, 0);
   return ATTN_OK;

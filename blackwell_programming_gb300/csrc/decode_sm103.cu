@@ -34,6 +34,14 @@
 // segment, K tiles through two rings), warp 4 = tcgen05 MMA issuer (whole
 // warp, one elected lane per instruction), warps 0-3 = the TMEM part of Q,
 // softmax (one row per thread), O rescale and epilogue.
+//
+// Copies are few and large: each TMA copy costs its issuing thread a few
+// hundred cycles of round trip, so the tensor maps see a [planes, rows, 576]
+// tensor as (64 features, rows, 9 chunks, planes) (the 128-byte chunk stride
+// inside the 1152-byte row stride) and one box of r rows x c chunks lands as c
+// consecutive r x 128-byte chunk images with the 128-byte swizzle, the layout
+// the MMA descriptors read.  A K tile then takes two or three copies instead
+// of nine.
 #include <cmath>
 #include <type_traits>
 
@@ -75,6 +83,8 @@ constexpr int B_QFULL = 0, B_QEMPTY = 1, B_QTFULL = 2, B_AFULL = 3, B_AEMPTY = B
 constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(Q_SMEM_CH == kLatentQChunks && BN == kLatentKeyRows && A_CH == B_CH + 1 && QCH == 2 * B_CH + 1,
+              "box shapes shared with the host");
 
 // TMEM: O half [0,256), S [256,320) (P as bf16 pairs in its first 32
 // columns), Q features 0..383 as bf16 pairs [320,512).
@@ -199,7 +209,8 @@ __device__ __forceinline__ int a_index(int c, int half) { return c < 4 * half ? 
 // latency.
 template <class P>
 __global__ void __launch_bounds__(kThreads, 1)
-    latent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, const P p) {
+    latent_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK5,
+                  const __grid_constant__ CUtensorMap tmK4, const __grid_constant__ CUtensorMap tmK1, const P p) {
   constexpr bool kPrefill = std::is_same<P, LatentPrefillParams>::value;
   using Walker = typename WalkerFor<P>::type;
   extern __shared__ uint8_t smem_raw[];
@@ -246,7 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmK5);
+      tma_prefetch_desc(&tmK4);
+      tma_prefetch_desc(&tmK1);
       // decode: each K tile is read by the two halves, then dead; prefill: K
       // is read again by every query head of its KV head and every block
       const uint64_t pol_k = kPrefill ? l2_policy_evict_last() : l2_policy_evict_first();
@@ -268,24 +281,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         qph ^= 1u;
         mbar_arrive_expect_tx(bar(B_QFULL), QS_BYTES);
         note_fill(0, qph ^ 1u);
-        for (int c = 0; c < Q_SMEM_CH; ++c)
-          tma_load_3d(sQ + c * CHUNK_Q, &tmQ, bar(B_QFULL), Q_TMEM_FEATS + c * 64, S.qrow0, S.qplane, pol_q);
+        tma_load_4d(sQ, &tmQ, bar(B_QFULL), 0, S.qrow0, Q_TMEM_FEATS / 64, S.qplane, pol_q);
         for (int j = 0; j < S.n; ++j) {
           const int y = (S.t0 + j) * BN;
           if (!(ok = mbar_wait(bar(B_AEMPTY + as), aph ^ 1u, wctx))) break;
           mbar_arrive_expect_tx(bar(B_AFULL + as), A_BYTES);
           note_fill(1 + as, aph);
-          for (int c = 0; c < QCH; ++c)
-            if (!in_ring_b(c, S.half))
-              tma_load_3d(sA + as * A_BYTES + a_index(c, S.half) * CHUNK_K, &tmK, bar(B_AFULL + as), c * 64, y,
-                          S.kplane, pol_k);
+          // ring A: the five chunks outside this item's value half (4..8 for
+          // half 0; 0..3 and 8 for half 1), in chunk order
+          if (S.half == 0) {
+            tma_load_4d(sA + as * A_BYTES, &tmK5, bar(B_AFULL + as), 0, y, B_CH, S.kplane, pol_k);
+          } else {
+            tma_load_4d(sA + as * A_BYTES, &tmK4, bar(B_AFULL + as), 0, y, 0, S.kplane, pol_k);
+            tma_load_4d(sA + as * A_BYTES + B_CH * CHUNK_K, &tmK1, bar(B_AFULL + as), 0, y, 2 * B_CH, S.kplane,
+                        pol_k);
+          }
           if (++as == AS) { as = 0; aph ^= 1u; }
           if (!(ok = mbar_wait(bar(B_BEMPTY + bs), bph ^ 1u, wctx))) break;
           mbar_arrive_expect_tx(bar(B_BFULL + bs), B_BYTES);
           note_fill(1 + AS + bs, bph);
-          for (int c = 0; c < B_CH; ++c)
-            tma_load_3d(sB + bs * B_BYTES + c * CHUNK_K, &tmK, bar(B_BFULL + bs), (4 * S.half + c) * 64, y, S.kplane,
-                        pol_k);
+          tma_load_4d(sB + bs * B_BYTES, &tmK4, bar(B_BFULL + bs), 0, y, B_CH * S.half, S.kplane, pol_k);
           if (++bs == BS) { bs = 0; bph ^= 1u; }
         }
       }
@@ -740,23 +755,22 @@ int decode_max_segments(int planes, int tiles, int grid) {
   return mx;
 }
 
-cudaError_t launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const DecodeParams& p, int grid,
-                          cudaStream_t stream) {
+cudaError_t launch_decode(const LatentMaps& m, const DecodeParams& p, int grid, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(latent_kernel<DecodeParams>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  latent_kernel<DecodeParams><<<grid, kThreads, SMEM_BYTES, stream>>>(tq, tk, p);
+  latent_kernel<DecodeParams><<<grid, kThreads, SMEM_BYTES, stream>>>(m.q, m.k5, m.k4, m.k1, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_latent_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const LatentPrefillParams& p,
-                                  int num_sms, cudaStream_t stream) {
+cudaError_t launch_latent_prefill(const LatentMaps& m, const LatentPrefillParams& p, int num_sms,
+                                  cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(latent_kernel<LatentPrefillParams>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
   const int grid = min(p.num_units, num_sms);
   if (grid <= 0) return cudaSuccess;
-  latent_kernel<LatentPrefillParams><<<grid, kThreads, SMEM_BYTES, stream>>>(tq, tk, p);
+  latent_kernel<LatentPrefillParams><<<grid, kThreads, SMEM_BYTES, stream>>>(m.q, m.k5, m.k4, m.k1, p);
   return cudaGetLastError();
 }
 

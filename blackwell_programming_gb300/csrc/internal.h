@@ -72,16 +72,27 @@ struct LatentPrefillParams {
   unsigned* err;
 };
 
-cudaError_t launch_latent_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const LatentPrefillParams& p,
-                                  int num_sms, cudaStream_t stream);
+// The latent kernel reads Q and K through tensor maps of a [planes, rows,
+// 576] bf16 tensor seen as (64 features, rows, 9 chunks of 64 features,
+// planes): Q in boxes of kLatentQRows rows x kLatentQChunks chunks (the
+// shared-memory part of Q, chunks 6..8), K in boxes of kLatentKeyRows keys x
+// 5, 4 or 1 chunks.
+constexpr int kLatentQRows = 128;
+constexpr int kLatentQChunks = 3;
+constexpr int kLatentKeyRows = 64;
+struct LatentMaps {
+  CUtensorMap q, k5, k4, k1;
+};
+
+cudaError_t launch_latent_prefill(const LatentMaps& m, const LatentPrefillParams& p, int num_sms,
+                                  cudaStream_t stream);
 
 // Number of partial slots each CTA needs for a grid of `grid` CTAs.
 int decode_max_segments(int planes, int tiles, int grid);
 int decode_tiles(int Nkv);
 int decode_key_tile();   // keys per K tile of the decode kernel (TMA box rows)
 
-cudaError_t launch_decode(const CUtensorMap& tq, const CUtensorMap& tk, const DecodeParams& p, int grid,
-                          cudaStream_t stream);
+cudaError_t launch_decode(const LatentMaps& m, const DecodeParams& p, int grid, cudaStream_t stream);
 
 // Merge the partials of every row into O [planes * group, 512] and LSE; O is
 // fp32 (o) or, when o is null, bf16 (o_bf16).
