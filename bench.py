@@ -151,9 +151,13 @@ class ClockSampler:
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample(wl, budget_s: float = 12.0):
-    """Time the fp64 oracle on whole (b, h) heads of the workload, bounded in time.
+    """Time the fp64 oracle on one (batch, head) problem of the workload,
+    repeated until the time budget is spent.
 
-    Returns (TFLOP/s, sample description, threads).  FLOPs of a head use the
+    The problem is a single head with the workload's shape and input
+    distribution (Nq x Nkv, d_qk, d_v, causal or not), drawn as its own
+    1-head workload; the oracle runs it whole each time.  Returns
+    (TFLOP/s, sample description, threads).  FLOPs of a head use the
     reported formula (4*Nq*Nkv*d, halved when causal; 2*Nq*Nkv*(d_qk+d_v)).
     """
     import numpy as np
@@ -181,9 +185,65 @@ def oracle_sample(wl, budget_s: float = 12.0):
         flops += per_head
         if elapsed >= budget_s or time.perf_counter() - t0 > 2 * budget_s:
             break
-    desc = "%d of %d (batch, head) pairs of %s, full rows, fp64 numpy%s" % (
-        done, len(rng_heads), wl.name, ", dropout %g" % DROPOUT if DROPOUT > 0.0 else "")
+    desc = ("one (batch, head) problem of %s's shape and distribution (%d x %d keys, d %d/%d%s), run %d times "
+            "(the workload has %d such problems), full rows, fp64 numpy%s") % (
+        wl.name, wl.Nq, wl.Nkv, wl.d_qk, wl.d_v, ", causal" if wl.causal else "", done, len(rng_heads),
+        ", dropout %g" % DROPOUT if DROPOUT > 0.0 else "")
     return flops / elapsed / 1e12, desc, cores
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def single_thread_oracle(names=("tile_d64", "causal_d64_bigq"), budget_s: float = 3.0):
+    """The fp64 oracle on whole small workloads in a child process whose BLAS
+    and OpenMP pools are limited to one thread:
+    {workload: {"tflops": ..., "seconds": ..., "runs": ...}}, or {} if the
+    child fails."""
+    code = (
+        "import json, sys, time\n"
+        "sys.path.insert(0, %r)\n"
+        "from blackwell_programming_gb300 import synthetic as syn\n"
+        "from oracle import attention\n"
+        "res = {}\n"
+        "for name in %r:\n"
+        "    wl = syn.WORKLOADS[name]\n"
+        "    q, k, v = syn.make_inputs(wl).f64()\n"
+        "    runs, t0 = 0, time.perf_counter()\n"
+        "    while True:\n"
+        "        attention(q, k, v, wl.causal, wl.scale)\n"
+        "        runs += 1\n"
+        "        if time.perf_counter() - t0 >= %r:\n"
+        "            break\n"
+        "    secs = (time.perf_counter() - t0) / runs\n"
+        "    res[name] = {'tflops': wl.flops / secs / 1e12, 'seconds': secs, 'runs': runs}\n"
+        "print(json.dumps(res))\n") % (ROOT, tuple(names), budget_s)
+    env = dict(os.environ)
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[var] = "1"
+    try:
+        out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                             timeout=60 + 10 * budget_s * len(names))
+        return json.loads(out.stdout.strip().splitlines()[-1]) if out.returncode == 0 else {}
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return {}
 
 
 def blas_threads() -> int:
@@ -222,7 +282,8 @@ def run_reference(args, wl):
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(wl),
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+                             "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": round(time.time() - t0, 1)}
     print(json.dumps(line), flush=True)
@@ -287,7 +348,134 @@ def measure_device(wl, steps, warmup, world, stream, flush, inputs):
         torch.cuda.synchronize()
         barrier(world)
     assert gb.attn_check_device(stream) == 0, "kernel reported a timed-out wait"
-    return [s.elapsed_time(e) / 1e3 for s, e in ev]
+    return [s.elapsed_time(e) / 1e3 for s, e in ev], o, lse
+
+
+# parity bar of the path (fp32 O against the fp64 oracle)
+O_MAX_ABS, O_MEAN_ABS, LSE_REL = 2e-2, 2e-3, 1e-3
+
+
+def sampled_parity(wl, inp, o, lse, heads: int = 6, rows: int = 48, seed: int = 1):
+    """The timed output against the fp64 oracle on sampled rows: `heads`
+    random (batch, query head) pairs (8 x `rows` of them for a one-query
+    decode), `rows` random query rows of each (all rows when Nq is smaller).  Returns max and mean |dO|, the max LSE error
+    relative to max(1, |LSE|), the rows checked and whether the bar holds."""
+    import numpy as np
+    from oracle import attention_head, kv_head_of
+    rng = np.random.default_rng(seed)
+    if wl.Nq == 1:
+        heads = max(heads, 8 * rows)     # decode: one row per head, so sample more heads
+    f64 = syn.bf16_bits_to_f64
+    dmax, dsum, n_el, lmax, n_rows = 0.0, 0.0, 0, 0.0, 0
+    for _ in range(heads):
+        b, h = int(rng.integers(wl.B)), int(rng.integers(wl.Hq))
+        g = kv_head_of(h, wl.Hq, wl.Hkv)
+        idx = np.sort(rng.choice(wl.Nq, size=min(rows, wl.Nq), replace=False))
+        q = f64(inp.q[b, h, idx])
+        k = f64(inp.k[b, g])
+        v = k[:, : wl.d_v] if inp.v is None else f64(inp.v[b, g])
+        o_ref, lse_ref = attention_head(q, k, v, wl.causal, wl.scale, row_index=idx, n_q=wl.Nq)
+        o_gpu = o[b, h, idx].float().cpu().numpy().astype(np.float64)
+        l_gpu = lse[b, h, idx].cpu().numpy().astype(np.float64)
+        d = np.abs(o_gpu - o_ref)
+        dmax, dsum, n_el = max(dmax, float(d.max())), dsum + float(d.sum()), n_el + d.size
+        fin = np.isfinite(lse_ref)
+        le = np.abs(l_gpu[fin] - lse_ref[fin]) / np.maximum(1.0, np.abs(lse_ref[fin]))
+        lmax = max(lmax, float(le.max()) if le.size else 0.0)
+        n_rows += len(idx)
+    mean = dsum / max(n_el, 1)
+    return {"max_abs_dO": dmax, "mean_abs_dO": mean, "max_lse_err": lmax, "rows": n_rows,
+            "bar": {"max_abs_dO": O_MAX_ABS, "mean_abs_dO": O_MEAN_ABS, "lse_rel": LSE_REL},
+            "ok": bool(dmax <= O_MAX_ABS and mean <= O_MEAN_ABS and lmax <= LSE_REL)}
+
+
+def link_bandwidth(nbytes: int = 256 << 20, reps: int = 5):
+    """Plain pinned host<->device copy bandwidth (GB/s, best of `reps`): host
+    to device, device to host, and both directions at once on two streams."""
+    import torch
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def best(fn):
+        t = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record()
+            fn()
+            for st in (s1, s2):
+                torch.cuda.current_stream().wait_stream(st)
+            b.record()
+            torch.cuda.synchronize()
+            t.append(a.elapsed_time(b) / 1e3)
+        return min(t)
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_in.copy_(h_in, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_out, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    return {"h2d_gbs": nbytes / best(h2d) / 1e9, "d2h_gbs": nbytes / best(d2h) / 1e9,
+            "bidir_gbs": 2 * nbytes / best(both) / 1e9, "bytes": nbytes}
+
+
+def roofline_for(wl, per_launch: float, peaks, peak_src: str):
+    """The roofline object of the attention workload's dominant kernel."""
+    flops = wl.flops
+    kind = ("decode" if wl.Nq == 1 else "latent_prefill") if wl.d_qk == 576 else "prefill"
+    if kind in ("prefill", "latent_prefill"):
+        achieved = flops / per_launch / 1e12
+        kname = {64: "prefill_kernel<64>", 128: "prefill_kernel<128>"}.get(wl.d_qk, "latent_kernel (prefill mode)")
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "peak_source": peak_src + " bf16_tflops (burst)",
+                "kernel": kname, "algorithmic_flops_per_launch": flops}
+    else:
+        achieved = algorithmic_bytes(wl) / per_launch / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_src + " hbm_gbs",
+                "kernel": "latent_kernel (decode mode) + combine_kernel (one step)",
+                "algorithmic_bytes_per_launch": algorithmic_bytes(wl),
+                "tensor_tflops": flops / per_launch / 1e12}
+    traffic_key = wl.name + ("_dropout%g" % DROPOUT if DROPOUT > 0.0 else "")
+    roof["traffic"] = committed_traffic(kind, traffic_key) if O_DTYPE == "fp32" else None
+    return roof, kind
+
+
+def device_inputs(wl):
+    """Seeded inputs of the workload: host bits, pinned host tensors and device tensors."""
+    import numpy as np
+    import torch
+    inp = syn.make_inputs(wl)
+    hq = torch.from_numpy(inp.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hk = torch.from_numpy(inp.k.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = None if inp.v is None else torch.from_numpy(inp.v.view(np.int16)).view(torch.bfloat16).pin_memory()
+    q, k = hq.cuda(), hk.cuda()
+    v = k[..., : wl.d_v] if hv is None else hv.cuda()
+    return inp, (hq, hk, hv), (q, k, v)
+
+
+def also_entry(name, steps, warmup, world, stream, flush, peaks, peak_src):
+    """Another workload of the path timed in the same run (device value,
+    roofline and sampled parity; no CPU or host-buffer legs)."""
+    wl = syn.WORKLOADS[name]
+    inp, _, dev = device_inputs(wl)
+    times, o, lse = measure_device(wl, steps, warmup, world, stream, flush, dev)
+    per_launch = reduce_max(sum(times), world) / steps
+    roof, _ = roofline_for(wl, per_launch, peaks, peak_src)
+    return {"workload": name, "config": workload_config(wl), "ms_per_step": per_launch * 1e3,
+            "value": aggregate(wl.flops, per_launch, world) / 1e12, "unit": "TFLOP/s", "roofline": roof,
+            "step_ms": {"min": min(times) * 1e3, "median": statistics.median(times) * 1e3, "max": max(times) * 1e3},
+            "parity": sampled_parity(wl, inp, o, lse), "gpu_launches": (2 if wl.Nq == 1 and wl.d_qk == 576 else 1) * steps}
 
 
 E2E_SCHEDULE = "per step: H2D of its inputs, the call, D2H of its results; three streams, two device slots"
@@ -391,27 +579,27 @@ def run_ours(args, wl):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, desc, cores = oracle_sample(wl, budget_s=args.ref_budget)
-        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc,
+               "cpu_model": cpu_model(), "single_thread": single_thread_oracle()}
 
-    inp = syn.make_inputs(wl)
-    import numpy as np
-    hq = torch.from_numpy(inp.q.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hk = torch.from_numpy(inp.k.view(np.int16)).view(torch.bfloat16).pin_memory()
-    hv = None if inp.v is None else torch.from_numpy(inp.v.view(np.int16)).view(torch.bfloat16).pin_memory()
-    q, k = hq.cuda(), hk.cuda()
-    v = k[..., : wl.d_v] if hv is None else hv.cuda()
+    inp, (hq, hk, hv), dev = device_inputs(wl)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.Stream()
+    peaks, peak_src = load_peaks()
+    also_names = [] if args.no_also else [n for n in args.also.split(",") if n and n != wl.name]
 
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     clocks = ClockSampler(int(vis[local]) if local < len(vis) and vis[local].strip().isdigit() else local)
     clocks.start()
-    times = measure_device(wl, args.steps, args.warmup, world, stream, flush, (q, k, v))
+    times, o, lse = measure_device(wl, args.steps, args.warmup, world, stream, flush, dev)
+    also = [also_entry(n, args.steps, args.warmup, world, stream, flush, peaks, peak_src) for n in also_names]
     clk = clocks.stop()
     total = sum(times)
     t_max = reduce_max(total, world)
     flops = wl.flops
     value = aggregate(flops * args.steps, t_max, world) / 1e12
+    parity = sampled_parity(wl, inp, o, lse) if rank == 0 else None
+    del o, lse
 
     e2e = None
     if not args.no_e2e:
@@ -419,36 +607,25 @@ def run_ours(args, wl):
         e2e_max = reduce_max(e2e_secs, world)
         e2e = {"value": aggregate(flops * args.steps, e2e_max, world) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "schedule": E2E_SCHEDULE}
+        link = link_bandwidth()
+        moved = (h2d + d2h) * args.steps / e2e_max / 1e9
+        e2e["link"] = dict(link, achieved_gbs=moved, frac_of_bidir=moved / link["bidir_gbs"])
 
-    peaks, peak_src = load_peaks()
-    kind = ("decode" if wl.Nq == 1 else "latent_prefill") if wl.d_qk == 576 else "prefill"
     per_launch = total / args.steps
-    if kind in ("prefill", "latent_prefill"):
-        achieved = flops / per_launch / 1e12
-        kname = {64: "prefill_kernel<64>", 128: "prefill_kernel<128>"}.get(wl.d_qk, "latent_kernel (prefill mode)")
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "peak_source": peak_src + " bf16_tflops (burst)",
-                "kernel": kname, "algorithmic_flops_per_launch": flops}
-    else:
-        achieved = algorithmic_bytes(wl) / per_launch / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_src + " hbm_gbs",
-                "kernel": "latent_kernel (decode mode) + combine_kernel (one step)",
-                "algorithmic_bytes_per_launch": algorithmic_bytes(wl),
-                "tensor_tflops": flops / per_launch / 1e12}
-    traffic_key = wl.name + ("_dropout%g" % DROPOUT if DROPOUT > 0.0 else "")
-    roof["traffic"] = committed_traffic(kind, traffic_key) if O_DTYPE == "fp32" else None
-    launches = (2 if kind == "decode" else 1) * args.steps
+    roof, kind = roofline_for(wl, per_launch, peaks, peak_src)
+    launches = (2 if kind == "decode" else 1) * args.steps + sum(a["gpu_launches"] for a in also)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": workload_config(wl), "roofline": roof, "cpu_baseline": cpu,
-                "e2e": e2e,
+                "e2e": e2e, "parity": parity,
                 "gpu_launches": launches, "clocks": clk,
                 "step_ms": {"min": min(times) * 1e3, "median": statistics.median(times) * 1e3,
                             "max": max(times) * 1e3}}
+        if also:
+            line["also"] = also
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -818,6 +995,11 @@ def main(argv=None):
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--also", default=None,
+                    help="comma-separated attention workloads also timed in the same run (device value, roofline, "
+                         "sampled parity); default: the long-context and decode workloads when the default "
+                         "workload runs unmodified")
+    ap.add_argument("--no-also", action="store_true", help="time the named workload only")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size (profiling cases)")
     ap.add_argument("--heads", type=int, default=None, help="override the workload's query heads (profiling cases)")
     ap.add_argument("--out", default="fp32", choices=["fp32", "bf16"], help="O output type (fp32 is the measured configuration)")
@@ -847,6 +1029,10 @@ def main(argv=None):
         wl = wl.with_sizes(B=args.batch, name="%s_B%d" % (wl.name, args.batch))
     if args.heads is not None:
         wl = wl.with_sizes(Hq=args.heads, name="%s_H%d" % (wl.name, args.heads))
+    if args.also is None:
+        plain = (args.workload == DEFAULT_WORKLOAD and args.batch is None and args.heads is None
+                 and DROPOUT == 0.0 and O_DTYPE == "fp32")
+        args.also = "long_causal_d128,decode_d576" if plain else ""
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)
