@@ -34,6 +34,7 @@ __device__ unsigned g_device_error[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 namespace {
 
 constexpr int kVersion = 100;
+constexpr int kDefaultExp2Split = 0;
 constexpr int kMaxDevices = 64;
 
 thread_local char t_cuda_error[256] = "";
@@ -206,6 +207,16 @@ bool env_flag(const char* name) {
   return s != nullptr && s[0] == '1';
 }
 
+// Share of the softmax's exponentials evaluated on the FMA pipe instead of
+// the SFU: ATTN_EXP2_SPLIT=4 or 8 puts one pair in four or eight there
+// (read at every call); anything else, or unset, keeps them all on the SFU.
+int exp2_split() {
+  const char* s = std::getenv("ATTN_EXP2_SPLIT");
+  if (s == nullptr) return kDefaultExp2Split;
+  const int v = std::atoi(s);
+  return (v == 4 || v == 8) ? v : 0;
+}
+
 bool check_env() {
   static const bool on = [] {
     const char* s = std::getenv("ATTN_CHECK");
@@ -327,6 +338,7 @@ int run_prefill(const void* q, const void* k, const void* v, float* o32, uint16_
   p.nqb = (Nq + 255) / 256;
   p.nkv_tiles = (Nkv + 127) / 128;
   p.num_units = B * Hq * p.nqb;
+  p.exp2_split = exp2_split();
   p.err = dev->err;
   cudaError_t e;
   if ((e = launch_prefill(d, tq, tk, tv, p, dev->num_sms, stream)) != cudaSuccess)

@@ -30,6 +30,9 @@ struct PrefillParams {
   // by drop_scale = 256 / (256 - drop_t) in the epilogue.
   uint32_t seed_lo, seed_hi, drop_t;
   float drop_scale;
+  // Exponentials on the FMA pipe: one pair in every exp2_split (0, 4 or 8;
+  // 0 = all on the SFU), dropout-free kernels only.
+  int exp2_split;
   int num_units;       // B * Hq * ceil(Nq / 256)
   int nqb;             // ceil(Nq / 256)
   int nkv_tiles;       // ceil(Nkv / 128)

@@ -154,7 +154,9 @@ __device__ __forceinline__ void keep_pair_masks(uint32_t f, uint32_t& m01, uint3
   asm("prmt.b32 %0, %1, 0, 0xAABB;" : "=r"(m23) : "r"(f));
 }
 
-template <int D, bool DROP>
+// SPLIT > 0: one exponential pair in every SPLIT on the FMA pipe (ex2_fma2),
+// the others on the SFU.
+template <int D, bool DROP, int SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -498,10 +500,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < BN / 4; ++i) {
             const int e = h * (BN / 4) + i;
             const uint64_t x = f2_fma(f2_pack(v[2 * e], v[2 * e + 1]), c2, nb2);
-            const float p0 = ex2(f2_lo(x));
-            const float p1 = ex2(f2_hi(x));
-            acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-            pk[i] = pack_bf16x2(p0, p1);
+            // ex2_fma2 gives 2^-125 rather than 0 for -inf, so masked tiles
+            // (where a row may see no key at all) keep every exponential on the SFU
+            uint64_t pp;
+            if (SPLIT > 0 && !need_mask && i % (SPLIT > 0 ? SPLIT : 1) == SPLIT - 1) {
+              pp = ex2_fma2(x);
+            } else {
+              pp = f2_pack(ex2(f2_lo(x)), ex2(f2_hi(x)));
+            }
+            acc[i & 3] = f2_add(acc[i & 3], pp);
+            pk[i] = pack_bf16x2(f2_lo(pp), f2_hi(pp));
           }
           if constexpr (DROP) {
             // dropout after the row sum: the normaliser counts every key,
@@ -590,11 +598,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool DROP>
+template <int D, bool DROP, int SPLIT>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                      int num_sms, cudaStream_t stream) {
   using C = Cfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, DROP, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   const int grid = min(p.num_units, num_sms);
@@ -602,9 +610,9 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   // The register split needs the kernel to be launched with enough registers;
   // otherwise setmaxnreg.inc could never be served, so refuse to launch.
   cudaFuncAttributes fa;
-  if ((e = cudaFuncGetAttributes(&fa, prefill_kernel<D, DROP>)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, prefill_kernel<D, DROP, SPLIT>)) != cudaSuccess) return e;
   if (((fa.numRegs + 7) / 8) * 8 < kRegsNeededAtLaunch) return cudaErrorInvalidConfiguration;
-  prefill_kernel<D, DROP><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  prefill_kernel<D, DROP, SPLIT><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -613,11 +621,20 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int num_sms, cudaStream_t stream) {
   const bool drop = p.drop_t != 0u;
-  if (d == 64) return drop ? launch_d<64, true>(tq, tk, tv, p, num_sms, stream)
-                           : launch_d<64, false>(tq, tk, tv, p, num_sms, stream);
-  if (d == 128) return drop ? launch_d<128, true>(tq, tk, tv, p, num_sms, stream)
-                            : launch_d<128, false>(tq, tk, tv, p, num_sms, stream);
-  return cudaErrorInvalidValue;
+  if (drop) {
+    if (d == 64) return launch_d<64, true, 0>(tq, tk, tv, p, num_sms, stream);
+    if (d == 128) return launch_d<128, true, 0>(tq, tk, tv, p, num_sms, stream);
+    return cudaErrorInvalidValue;
+  }
+  switch (d * 100 + p.exp2_split) {
+    case 6400: return launch_d<64, false, 0>(tq, tk, tv, p, num_sms, stream);
+    case 6404: return launch_d<64, false, 4>(tq, tk, tv, p, num_sms, stream);
+    case 6408: return launch_d<64, false, 8>(tq, tk, tv, p, num_sms, stream);
+    case 12800: return launch_d<128, false, 0>(tq, tk, tv, p, num_sms, stream);
+    case 12804: return launch_d<128, false, 4>(tq, tk, tv, p, num_sms, stream);
+    case 12808: return launch_d<128, false, 8>(tq, tk, tv, p, num_sms, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace gbattn

@@ -511,6 +511,35 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
+// 2^x for two fp32 values packed in one 64-bit register (low word first), on
+// the FMA pipe instead of the SFU: the FMA half of the softmax's SFU/FMA split
+// of its exponentials ("Distilling a 4.5 hour CUDA talk", section 2: the SFU's
+// EX2 runs at a fraction of the FMA rate).  Cody-Waite style reduction:
+// n = x rounded to the nearest integer (adding and subtracting 1.5 * 2^23),
+// f = x - n in [-1/2, 1/2]; 2^f by a degree-3 polynomial fitted to 2^f on
+// [-1/2, 1/2] by weighted least squares on Chebyshev nodes (iterated toward
+// the minimax fit; relative error below 7.5e-5, about 2^-13.7); 2^n added to
+// the exponent field as an integer.  x is clamped at -125, so arguments
+// below it give 2^-125 ~ 2.4e-38 instead of 0: next to a row maximum of at
+// least 1 such weights vanish below fp32's resolution of the row sum and of
+// O.  -inf (a masked key) also gives 2^-125, so callers keep masked tiles,
+// where a row may see no key at all, on the SFU.
+__device__ __forceinline__ uint64_t ex2_fma2(uint64_t x2) {
+  constexpr float kRound = 12582912.f;   // 1.5 * 2^23
+  constexpr float c0 = 9.999280736e-01f, c1 = 6.932609862e-01f, c2 = 2.426111219e-01f, c3 = 5.517166493e-02f;
+  const uint64_t x = f2_pack(fmaxf(f2_lo(x2), -125.f), fmaxf(f2_hi(x2), -125.f));
+  const uint64_t t = f2_add(x, f2_pack(kRound, kRound));          // magic + n
+  const uint64_t n = f2_add(t, f2_pack(-kRound, -kRound));        // n
+  const uint64_t f = f2_fma(n, f2_pack(-1.f, -1.f), x);           // x - n
+  uint64_t q = f2_fma(f2_pack(c3, c3), f, f2_pack(c2, c2));
+  q = f2_fma(q, f, f2_pack(c1, c1));
+  q = f2_fma(q, f, f2_pack(c0, c0));
+  // the low mantissa bits of t hold n: shifted into the exponent field
+  const uint32_t lo = static_cast<uint32_t>(q) + (static_cast<uint32_t>(t) << 23);
+  const uint32_t hi = static_cast<uint32_t>(q >> 32) + (static_cast<uint32_t>(t >> 32) << 23);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 // Per-warpgroup register split (setmaxnreg): the counts must be multiples of
 // 8 in [24, 256] and every warp of the warpgroup must execute the same one.
 template <uint32_t N>
