@@ -335,7 +335,10 @@ int run_prefill(const void* q, const void* k, const void* v, float* o32, uint16_
   p.seed_hi = static_cast<uint32_t>(drop.seed >> 32);
   p.drop_t = drop.t;
   p.drop_scale = static_cast<float>(256.0 / (256.0 - static_cast<double>(drop.t)));
-  p.nqb = (Nq + 255) / 256;
+  // Two 128-row tiles per unit (they ping-pong on the tensor core); one when
+  // two-tile units would leave SMs idle, so that more SMs share the work.
+  p.tiles_per_unit = (static_cast<long long>(B) * Hq * ((Nq + 255) / 256) < dev->num_sms) ? 1 : 2;
+  p.nqb = (Nq + 128 * p.tiles_per_unit - 1) / (128 * p.tiles_per_unit);
   p.nkv_tiles = (Nkv + 127) / 128;
   p.num_units = B * Hq * p.nqb;
   p.exp2_split = exp2_split();

@@ -33,8 +33,9 @@ struct PrefillParams {
   // Exponentials on the FMA pipe: one pair in every exp2_split (0, 4 or 8;
   // 0 = all on the SFU), dropout-free kernels only.
   int exp2_split;
-  int num_units;       // B * Hq * ceil(Nq / 256)
-  int nqb;             // ceil(Nq / 256)
+  int tiles_per_unit;  // 128-row query tiles per work unit: 2, or 1 for problems under one wave
+  int num_units;       // B * Hq * nqb
+  int nqb;             // ceil(Nq / (128 * tiles_per_unit))
   int nkv_tiles;       // ceil(Nkv / 128)
   unsigned* err;       // device error word
 };

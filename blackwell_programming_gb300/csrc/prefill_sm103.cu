@@ -85,8 +85,9 @@ struct Cfg {
 };
 
 struct Unit {
-  int b, h, qb;
-  int n[2];   // K/V tiles visited by query tile 0 / 1
+  int b, h;
+  int row0[2];   // first query row of tile 0 / 1 (Nq: the tile does not exist)
+  int n[2];      // K/V tiles visited by query tile 0 / 1
 };
 
 __device__ __forceinline__ int kv_tiles_for(int q0, const PrefillParams& p) {
@@ -99,17 +100,26 @@ __device__ __forceinline__ int kv_tiles_for(int q0, const PrefillParams& p) {
 }
 
 // Unit u: query-block index descending (longest causal work first), then
-// (batch, head) with the heads of one KV group adjacent.
+// (batch, head) with the heads of one KV group adjacent.  A block is two
+// 128-row tiles, or one when the problem has fewer two-tile blocks than the
+// GPU has SMs (then tile 1 does not exist and its warps idle).
 __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p) {
   Unit U;
   const int bh_count = p.B * p.Hq;
   const int qb_rev = u / bh_count;
   const int bh = u - qb_rev * bh_count;
-  U.qb = p.nqb - 1 - qb_rev;
+  const int qb = p.nqb - 1 - qb_rev;
   U.b = bh / p.Hq;
   U.h = bh - U.b * p.Hq;
-  U.n[0] = kv_tiles_for(U.qb * 2 * BM, p);
-  U.n[1] = kv_tiles_for(U.qb * 2 * BM + BM, p);
+  if (p.tiles_per_unit == 1) {
+    U.row0[0] = qb * BM;
+    U.row0[1] = p.Nq;
+  } else {
+    U.row0[0] = qb * 2 * BM;
+    U.row0[1] = qb * 2 * BM + BM;
+  }
+  U.n[0] = kv_tiles_for(U.row0[0], p);
+  U.n[1] = kv_tiles_for(U.row0[1], p);
   return U;
 }
 
@@ -236,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           qph ^= 1u << t;
           mbar_arrive_expect_tx(bar(C::B_QFULL + t), C::Q_BYTES);
           note_fill(t, ((qph >> t) & 1u) ^ 1u);
-          const int qrow = (U.qb * 2 + t) * BM;
+          const int qrow = U.row0[t];
           for (int kc = 0; kc < C::KCH; ++kc)
             tma_load_4d(sQ + t * C::Q_BYTES + kc * C::CHUNK_Q, &tmQ, bar(C::B_QFULL + t), kc * 64,
                         p.token_major ? U.h : qrow, p.token_major ? qrow : U.h, U.b, pol_q);
@@ -412,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (u >= p.num_units) break;
       const Unit U = decode_unit(u, p);
       const int n = t ? U.n[1] : U.n[0];
-      const int q0 = (U.qb * 2 + t) * BM;
+      const int q0 = U.row0[t];
       const int row = q0 + row_in_tile;
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;

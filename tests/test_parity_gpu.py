@@ -74,6 +74,13 @@ SMALL = [
       scale=1 / math.sqrt(192), v_aliases_k=True),
     W("latent_prefill_zero_scale", B=1, Hq=1, Hkv=1, Nq=200, Nkv=200, d_qk=576, d_v=512, causal=True,
       scale=0.0, v_aliases_k=True),
+    # at least as many two-tile units as the GPU has SMs: two 128-row tiles per
+    # unit (smaller problems above run one tile per unit); ragged tails and
+    # causal rows that see no key in that mode
+    W("two_tile_units_ragged_d64", B=1, Hq=152, Hkv=38, Nq=200, Nkv=200, d_qk=64, d_v=64, causal=False,
+      scale=0.125),
+    W("two_tile_units_causal_nq_gt_nkv_d128", B=2, Hq=80, Hkv=20, Nq=300, Nkv=129, d_qk=128, d_v=128, causal=True,
+      scale=0.088),
     # one query but 256 query heads per KV head: more rows than a decode tile, so prefill mode
     W("latent_one_query_many_heads", B=1, Hq=256, Hkv=1, Nq=1, Nkv=200, d_qk=576, d_v=512, causal=False,
       scale=1 / math.sqrt(192), v_aliases_k=True),
