@@ -35,6 +35,7 @@ namespace {
 
 constexpr int kVersion = 100;
 constexpr int kDefaultExp2Split = 0;
+constexpr int kGemmGroupM = 16;   // row blocks of 256 per raster group of the CTA-pair GEMM
 constexpr int kMaxDevices = 64;
 
 thread_local char t_cuda_error[256] = "";
@@ -490,6 +491,11 @@ int gemm_bf16_nt(const void* a, const void* b, void* c, int M, int N, int K, int
   p.tiles_m = (M + rows_per_tile - 1) / rows_per_tile;
   p.tiles_n = (N + gemm_tile_cols() - 1) / gemm_tile_cols();
   p.num_tiles = p.tiles_m * p.tiles_n;
+  {
+    const char* s = std::getenv("ATTN_GEMM_GROUP_M");
+    const int g = s != nullptr ? std::atoi(s) : 0;
+    p.group_m = (g >= 1 && g <= 1024) ? g : kGemmGroupM;
+  }
   p.err = dev->err;
   cudaError_t e;
   if ((e = use_pair ? launch_gemm_pair(ta, tb, p, dev->num_sms, stream) : launch_gemm(ta, tb, p, dev->num_sms, stream)) !=

@@ -230,7 +230,6 @@ constexpr int BM = 128;           // rows per CTA (the pair covers 256)
 constexpr int BN = 256;           // columns per pair tile
 constexpr int BNH = 128;          // rows of B each CTA loads
 constexpr int kStages = 6;
-constexpr int kGroupM = 8;        // row blocks of 256 per raster group
 constexpr uint32_t A_BYTES = BM * BK * 2;    // 16 KB
 constexpr uint32_t B_BYTES = BNH * BK * 2;   // 16 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -242,11 +241,14 @@ constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN, false, false);
 
+// Tile t -> (256-row block, column block): groups of p.group_m row blocks,
+// all column blocks of a group before the next, the row block fastest inside
+// a group (a group's A rows stay in L2 while B's columns stream past them).
 __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb, int& nb) {
-  const int per_group = kGroupM * p.tiles_n;
+  const int per_group = p.group_m * p.tiles_n;
   const int g = t / per_group;
-  const int first = g * kGroupM;
-  const int gsize = min(p.tiles_m - first, kGroupM);
+  const int first = g * p.group_m;
+  const int gsize = min(p.tiles_m - first, p.group_m);
   const int in = t - g * per_group;
   mb = first + in % gsize;
   nb = in / gsize;

@@ -110,6 +110,7 @@ struct GemmParams {
   int M, N, K;
   int c_fp32;          // 1: C is fp32, 0: bf16
   int tiles_m, tiles_n, num_tiles;
+  int group_m;         // CTA-pair kernel: 256-row blocks per raster group
   unsigned* err;
 };
 
