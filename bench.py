@@ -374,7 +374,12 @@ def sampled_parity(wl, inp, o, lse, heads: int = 6, rows: int = 48, seed: int = 
         q = f64(inp.q[b, h, idx])
         k = f64(inp.k[b, g])
         v = k[:, : wl.d_v] if inp.v is None else f64(inp.v[b, g])
-        o_ref, lse_ref = attention_head(q, k, v, wl.causal, wl.scale, row_index=idx, n_q=wl.Nq)
+        if DROPOUT > 0.0:
+            from oracle.dropout_fp64 import attention_dropout_head
+            o_ref, lse_ref = attention_dropout_head(q, k, v, wl.causal, wl.scale, DROPOUT, DROPOUT_SEED, b, h,
+                                                    row_index=idx, n_q=wl.Nq)
+        else:
+            o_ref, lse_ref = attention_head(q, k, v, wl.causal, wl.scale, row_index=idx, n_q=wl.Nq)
         o_gpu = o[b, h, idx].float().cpu().numpy().astype(np.float64)
         l_gpu = lse[b, h, idx].cpu().numpy().astype(np.float64)
         d = np.abs(o_gpu - o_ref)
@@ -384,9 +389,14 @@ def sampled_parity(wl, inp, o, lse, heads: int = 6, rows: int = 48, seed: int = 
         lmax = max(lmax, float(le.max()) if le.size else 0.0)
         n_rows += len(idx)
     mean = dsum / max(n_el, 1)
-    return {"max_abs_dO": dmax, "mean_abs_dO": mean, "max_lse_err": lmax, "rows": n_rows,
-            "bar": {"max_abs_dO": O_MAX_ABS, "mean_abs_dO": O_MEAN_ABS, "lse_rel": LSE_REL},
-            "ok": bool(dmax <= O_MAX_ABS and mean <= O_MEAN_ABS and lmax <= LSE_REL)}
+    # with dropout, kept weights are scaled by the keep factor, and so is the O bar
+    f = 1.0
+    if DROPOUT > 0.0:
+        from oracle.dropout_fp64 import drop_threshold, keep_scale
+        f = keep_scale(drop_threshold(DROPOUT))
+    bar = {"max_abs_dO": O_MAX_ABS * f, "mean_abs_dO": O_MEAN_ABS * f, "lse_rel": LSE_REL}
+    return {"max_abs_dO": dmax, "mean_abs_dO": mean, "max_lse_err": lmax, "rows": n_rows, "bar": bar,
+            "ok": bool(dmax <= bar["max_abs_dO"] and mean <= bar["mean_abs_dO"] and lmax <= LSE_REL)}
 
 
 def link_bandwidth(nbytes: int = 256 << 20, reps: int = 5):
