@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libgbattn.so")
 STAMP = os.path.join(LIBDIR, "host_arch.txt")
-SOURCES = ["attn_api.cu", "prefill_sm103.cu", "decode_sm103.cu", "gemm_sm103.cu"]
+SOURCES = ["attn_api.cu", "prefill_sm103.cu", "decode_sm103.cu", "decode_pair_sm103.cu", "gemm_sm103.cu"]
 HEADERS = [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "philox.cuh"),
            os.path.join(ROOT, "include", "gbattn.h"), os.path.join(ROOT, "include", "gbgemm.h"),
            os.path.join(ROOT, "include", "gblayer.h")]

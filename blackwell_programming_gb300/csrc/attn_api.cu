@@ -57,6 +57,9 @@ struct DeviceInfo {
   // (which the default pool does, at about 0.1 ms per call for a 40 MB
   // workspace).
   cudaMemPool_t pool = nullptr;
+  // Clusters of the CTA-pair decode kernel that fit on the device at once
+  // (-1 until first asked).
+  int decode_pairs = -1;
 };
 
 std::mutex g_mu;
@@ -201,6 +204,103 @@ int make_latent_maps(LatentMaps* m, const void* q, uint64_t q_rows, uint64_t q_p
   return make_map4(&m->k1, k, kd, ks, kLatentKeyRows, 1);
 }
 
+// The CTA-pair decode's maps: Q [planes, group, 576] in boxes of 128 rows x
+// 1 chunk, and over K [planes, Nkv, 576] the score CTA's boxes of 64 keys x 3
+// chunks and the value CTA's of 64 keys x 8 chunks (V).
+int make_pair_maps(CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, const void* q, uint64_t group,
+                   const void* k, uint64_t k_rows, uint64_t planes) {
+  const uint64_t row = 576 * 2;
+  const uint64_t qd[4] = {64, group, 9, planes};
+  const uint64_t qs[3] = {row, 128, row * group};
+  const uint64_t kd[4] = {64, k_rows, 9, planes};
+  const uint64_t ks[3] = {row, 128, row * k_rows};
+  int st;
+  if ((st = make_map4(tq, q, qd, qs, 128, 1)) != ATTN_OK) return st;
+  if ((st = make_map4(tk, k, kd, ks, kLatentKeyRows, kPairKeyChunks)) != ATTN_OK) return st;
+  return make_map4(tv, k, kd, ks, kLatentKeyRows, kPairValueChunks);
+}
+
+// Which split-KV decode kernel runs: the CTA-pair kernel (score and value
+// CTAs), or with ATTN_DECODE=single the one-CTA kernel that computes the
+// score tile in both O halves (read at every call).
+bool decode_use_pair() {
+  const char* s = std::getenv("ATTN_DECODE");
+  return !(s != nullptr && std::strcmp(s, "single") == 0);
+}
+
+// Shape of one split-KV decode launch: the kernel, its CTAs (single) or
+// clusters (pair), and the workspace its partials need.
+struct DecodePlan {
+  bool pair = false;
+  int grid = 0;          // CTAs (single) or CTA pairs (pair)
+  int max_seg = 0;       // single: partial slots per CTA
+  size_t rows = 0;       // partial rows (slots x 128)
+  int cols = 0;          // partial O columns per row
+  size_t floats() const { return rows * static_cast<size_t>(cols + 1); }
+};
+
+int plan_decode(DeviceInfo* dev, int planes, int tiles, DecodePlan* out) {
+  DecodePlan pl;
+  pl.pair = decode_use_pair();
+  if (pl.pair) {
+    {
+      std::lock_guard<std::mutex> lock(g_mu);
+      if (dev->decode_pairs < 0) {
+        int n = 0;
+        const int e = decode_pair_max_pairs(dev->num_sms, &n);
+        if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "cudaOccupancyMaxActiveClusters");
+        dev->decode_pairs = n;
+      }
+    }
+    if (dev->decode_pairs <= 0) return ATTN_ERR_UNSUPPORTED;
+    const long long total = static_cast<long long>(planes) * tiles;
+    pl.grid = static_cast<int>(std::min<long long>(total, std::min(dev->decode_pairs, dev->num_sms / 2)));
+    pl.rows = static_cast<size_t>(decode_pair_slots(planes, pl.grid)) * 128;
+    pl.cols = 512;
+  } else {
+    const long long total = 2LL * planes * tiles;
+    pl.grid = static_cast<int>(std::min<long long>(total, dev->num_sms));
+    pl.max_seg = decode_max_segments(planes, tiles, pl.grid);
+    pl.rows = static_cast<size_t>(pl.grid) * pl.max_seg * 128;
+    pl.cols = 256;
+  }
+  *out = pl;
+  return ATTN_OK;
+}
+
+// The decode kernel and the combine of `pl` on checked arguments; `ws` holds
+// pl.floats() floats.
+int launch_decode_plan(const DecodePlan& pl, const void* q, const void* k, float* o32, uint16_t* o16, float* lse,
+                       int group, int planes, int Nkv, float scale_log2, float* ws, DeviceInfo* dev,
+                       cudaStream_t stream) {
+  DecodeParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.planes = planes;
+  p.group = group;
+  p.Nkv = Nkv;
+  p.tiles = decode_tiles(Nkv);
+  p.max_seg = pl.max_seg;
+  p.scale_log2 = scale_log2;
+  p.err = dev->err;
+  p.o_part = ws;
+  p.lse_part = ws + pl.rows * static_cast<size_t>(pl.cols);
+  int st;
+  cudaError_t e;
+  if (pl.pair) {
+    CUtensorMap tq, tk, tv;
+    if ((st = make_pair_maps(&tq, &tk, &tv, q, group, k, Nkv, planes)) != ATTN_OK) return st;
+    if ((e = launch_decode_pair(tq, tk, tv, p, pl.grid, stream)) != cudaSuccess) return cuda_fail(e, "decode launch");
+    if ((e = launch_combine_pair(p, pl.grid, o32, o16, lse, stream)) != cudaSuccess)
+      return cuda_fail(e, "combine launch");
+    return ATTN_OK;
+  }
+  LatentMaps maps;
+  if ((st = make_latent_maps(&maps, q, group, planes, k, Nkv, planes)) != ATTN_OK) return st;
+  if ((e = launch_decode(maps, p, pl.grid, stream)) != cudaSuccess) return cuda_fail(e, "decode launch");
+  if ((e = launch_combine(p, pl.grid, o32, o16, lse, stream)) != cudaSuccess) return cuda_fail(e, "combine launch");
+  return ATTN_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool env_flag(const char* name) {
@@ -270,12 +370,9 @@ size_t attn_decode_workspace_bytes(int B, int Hkv, int Nkv) {
   if (B <= 0 || Hkv <= 0 || Nkv <= 0) return 0;
   DeviceInfo* d = nullptr;
   if (device_info(&d) != ATTN_OK) return 0;
-  const int planes = B * Hkv;
-  const int tiles = decode_tiles(Nkv);
-  const long long total = 2LL * planes * tiles;
-  const int grid = static_cast<int>(std::min<long long>(total, d->num_sms));
-  const int ms = decode_max_segments(planes, tiles, grid);
-  return static_cast<size_t>(grid) * ms * 128 * (256 + 1) * sizeof(float);
+  DecodePlan pl;
+  if (plan_decode(d, B * Hkv, decode_tiles(Nkv), &pl) != ATTN_OK) return 0;
+  return pl.floats() * sizeof(float);
 }
 
 int attn_check_device(attn_stream_t stream, int reset) {
@@ -419,34 +516,17 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint1
   } else {
     const int group = Hq / Hkv;
     const int planes = B * Hkv;
-    LatentMaps maps;
-    if ((st = make_latent_maps(&maps, q, group, planes, k, Nkv, planes)) != ATTN_OK) return st;
-    DecodeParams p{};
-    p.q = static_cast<const uint16_t*>(q);
-    p.planes = planes;
-    p.group = group;
-    p.Nkv = Nkv;
-    p.tiles = decode_tiles(Nkv);
-    p.scale_log2 = scale_log2;
-    p.err = dev->err;
-    const long long total = 2LL * planes * p.tiles;
-    const int grid = static_cast<int>(std::min<long long>(total, dev->num_sms));
-    p.max_seg = decode_max_segments(planes, p.tiles, grid);
-    const size_t n_slots = static_cast<size_t>(grid) * p.max_seg * 128;
+    DecodePlan pl;
+    if ((st = plan_decode(dev, planes, decode_tiles(Nkv), &pl)) != ATTN_OK) return st;
     cudaMemPool_t pool = nullptr;
     if ((st = decode_pool(dev, &pool)) != ATTN_OK) return st;
     void* ws = nullptr;
-    if ((e = cudaMallocFromPoolAsync(&ws, n_slots * (256 + 1) * sizeof(float), pool, stream)) != cudaSuccess)
+    if ((e = cudaMallocFromPoolAsync(&ws, pl.floats() * sizeof(float), pool, stream)) != cudaSuccess)
       return cuda_fail(e, "cudaMallocFromPoolAsync(decode workspace)");
-    p.o_part = static_cast<float*>(ws);
-    p.lse_part = p.o_part + n_slots * 256;
-    if ((e = launch_decode(maps, p, grid, stream)) != cudaSuccess) {
+    if ((st = launch_decode_plan(pl, q, k, o32, o16, lse, group, planes, Nkv, scale_log2, static_cast<float*>(ws),
+                                 dev, stream)) != ATTN_OK) {
       cudaFreeAsync(ws, stream);
-      return cuda_fail(e, "decode launch");
-    }
-    if ((e = launch_combine(p, grid, o32, o16, lse, stream)) != cudaSuccess) {
-      cudaFreeAsync(ws, stream);
-      return cuda_fail(e, "combine launch");
+      return st;
     }
     if ((e = cudaFreeAsync(ws, stream)) != cudaSuccess) return cuda_fail(e, "cudaFreeAsync(decode workspace)");
   }
@@ -650,33 +730,19 @@ extern "C" int attn_decode_fwd_noalloc(const void* q, const void* kv, float* o, 
 
   const int group = Hq / Hkv;
   const int planes = B * Hkv;
-  DecodeParams p{};
-  p.q = static_cast<const uint16_t*>(q);
-  p.planes = planes;
-  p.group = group;
-  p.Nkv = Nkv;
-  p.tiles = decode_tiles(Nkv);
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.err = dev->err;
-  const long long total = 2LL * planes * p.tiles;
-  const int grid = static_cast<int>(std::min<long long>(total, dev->num_sms));
-  p.max_seg = decode_max_segments(planes, p.tiles, grid);
-  const size_t n_slots = static_cast<size_t>(grid) * p.max_seg * 128;
-  if (n_slots * (256 + 1) * sizeof(float) > kNoAllocScratchBytes) {
-    std::snprintf(t_cuda_error, sizeof(t_cuda_error),
-                  "needs %zu bytes of scratch, the static array holds %zu", n_slots * (256 + 1) * sizeof(float),
+  DecodePlan pl;
+  if ((st = plan_decode(dev, planes, decode_tiles(Nkv), &pl)) != ATTN_OK) return st;
+  const size_t need = pl.floats() * sizeof(float);
+  if (need > kNoAllocScratchBytes) {
+    std::snprintf(t_cuda_error, sizeof(t_cuda_error), "needs %zu bytes of scratch, the static array holds %zu", need,
                   kNoAllocScratchBytes);
     return ATTN_ERR_SCRATCH_LIMIT;
   }
-  LatentMaps maps;
-  if ((st = make_latent_maps(&maps, q, group, planes, kv, Nkv, planes)) != ATTN_OK) return st;
   // Every slot the combine kernel reads is written first by the decode
   // kernel in the same call, so nothing needs clearing between calls.
-  p.o_part = scratch;
-  p.lse_part = scratch + n_slots * 256;
-  cudaError_t e;
-  if ((e = launch_decode(maps, p, grid, stream)) != cudaSuccess) return cuda_fail(e, "decode launch");
-  if ((e = launch_combine(p, grid, o, nullptr, lse, stream)) != cudaSuccess) return cuda_fail(e, "combine launch");
+  if ((st = launch_decode_plan(pl, q, kv, o, nullptr, lse, group, planes, Nkv, scale * 1.4426950408889634f, scratch,
+                               dev, stream)) != ATTN_OK)
+    return st;
   if (check_env()) return read_device_error(stream, dev->err, 0);
   return ATTN_OK;
 }

@@ -91,6 +91,25 @@ struct LatentMaps {
 cudaError_t launch_latent_prefill(const LatentMaps& m, const LatentPrefillParams& p, int num_sms,
                                   cudaStream_t stream);
 
+// The CTA-pair decode (decode_pair_sm103.cu): one CTA of each cluster of two
+// computes the score tiles and the softmax, the other holds O and computes
+// P V.  K is read through the same 4-D view as above, in boxes of
+// kLatentKeyRows keys x kPairKeyChunks chunks (score CTA) and x
+// kPairValueChunks chunks (value CTA: V, the first 512 features), and Q in
+// boxes of 128 rows x 1 chunk (rows past the group read as zeros).  The
+// pieces go to decode_pair_slots(planes, pairs) slots of [128, 512] floats
+// and 128 LSEs, which launch_combine_pair merges.
+constexpr int kPairKeyChunks = 3;
+constexpr int kPairValueChunks = 8;
+int decode_pair_slots(int planes, int pairs);
+// Clusters of the pair kernel that fit on the device at once (0 on success).
+int decode_pair_max_pairs(int num_sms, int* out);
+// `tq` maps Q [planes, group, 576] in boxes of 128 rows x 1 chunk.
+cudaError_t launch_decode_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeParams& p, int pairs, cudaStream_t stream);
+cudaError_t launch_combine_pair(const DecodeParams& p, int pairs, float* o, uint16_t* o_bf16, float* lse,
+                                cudaStream_t stream);
+
 // Number of partial slots each CTA needs for a grid of `grid` CTAs.
 int decode_max_segments(int planes, int tiles, int grid);
 int decode_tiles(int Nkv);

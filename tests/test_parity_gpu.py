@@ -84,7 +84,25 @@ SMALL = [
     # one query but 256 query heads per KV head: more rows than a decode tile, so prefill mode
     W("latent_one_query_many_heads", B=1, Hq=256, Hkv=1, Nq=1, Nkv=200, d_qk=576, d_v=512, causal=False,
       scale=1 / math.sqrt(192), v_aliases_k=True),
+    # decode with large logits: rows raise their reference mid-sequence, so O
+    # is rescaled between key tiles; a full 128-head tile and a ragged tail
+    W("decode_large_logits", B=4, Hq=128, Hkv=1, Nq=1, Nkv=2000, d_qk=576, d_v=512, causal=False,
+      scale=1 / math.sqrt(192), v_aliases_k=True, q_factor=8.0),
+    # more sequences than CTA pairs: many sequences lie inside one pair's
+    # range and are written out whole, the others are merged from two pieces
+    W("decode_whole_sequences", B=96, Hq=16, Hkv=1, Nq=1, Nkv=256, d_qk=576, d_v=512, causal=False,
+      scale=1 / math.sqrt(192), v_aliases_k=True),
 ]
+
+DECODE = [w for w in SMALL if w.d_qk == 576 and w.Nq == 1 and w.Hq // w.Hkv <= 128]
+
+
+@pytest.mark.parametrize("wl", DECODE, ids=lambda w: w.name)
+def test_decode_one_cta_kernel_full_parity(wl, monkeypatch):
+    """The one-CTA decode kernel (ATTN_DECODE=single), kept for comparison,
+    meets the same parity bar as the default CTA-pair kernel."""
+    monkeypatch.setenv("ATTN_DECODE", "single")
+    full_case(wl)
 
 
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
