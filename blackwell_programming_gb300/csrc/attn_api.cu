@@ -204,8 +204,8 @@ int make_latent_maps(LatentMaps* m, const void* q, uint64_t q_rows, uint64_t q_p
   return make_map4(&m->k1, k, kd, ks, kLatentKeyRows, 1);
 }
 
-// The CTA-pair decode's maps: Q [planes, group, 576] in boxes of 128 rows x
-// 1 chunk, and over K [planes, Nkv, 576] the score CTA's boxes of 64 keys x 3
+// The CTA-pair decode's maps: Q [planes, group, 576] in boxes of 64 rows x 3
+// chunks, and over K [planes, Nkv, 576] the score CTA's boxes of 64 keys x 3
 // chunks and the value CTA's of 64 keys x 8 chunks (V).
 int make_pair_maps(CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, const void* q, uint64_t group,
                    const void* k, uint64_t k_rows, uint64_t planes) {
@@ -215,7 +215,7 @@ int make_pair_maps(CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, const void
   const uint64_t kd[4] = {64, k_rows, 9, planes};
   const uint64_t ks[3] = {row, 128, row * k_rows};
   int st;
-  if ((st = make_map4(tq, q, qd, qs, 128, 1)) != ATTN_OK) return st;
+  if ((st = make_map4(tq, q, qd, qs, kLatentKeyRows, kPairKeyChunks)) != ATTN_OK) return st;
   if ((st = make_map4(tk, k, kd, ks, kLatentKeyRows, kPairKeyChunks)) != ATTN_OK) return st;
   return make_map4(tv, k, kd, ks, kLatentKeyRows, kPairValueChunks);
 }

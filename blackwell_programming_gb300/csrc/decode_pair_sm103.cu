@@ -53,6 +53,7 @@ constexpr int BN = 64;                  // keys per K tile
 constexpr int KCH = DQK / 64;           // 9 chunks of 64 features (128 bytes)
 constexpr int GCH = kPairKeyChunks;     // chunks per K granule (one TMA box)
 constexpr int GRANS = KCH / GCH;        // granules per K tile
+constexpr int QPOS = 2 * GRANS;         // ring positions of a segment's Q: 2 halves of 64 rows x GRANS chunk groups
 constexpr int KSLOTS = 7;               // score CTA: K granule ring
 constexpr int NSTG = 2;                 // score CTA: P staging buffers
 constexpr int VST = 2;                  // value CTA: V stages
@@ -69,7 +70,6 @@ constexpr uint32_t kFull = 0xFFFFFFFFu;
 
 constexpr uint32_t CHUNK_K = BN * 128;            // 8 KB: 64 keys x 64 features
 constexpr uint32_t GRAN_BYTES = GCH * CHUNK_K;    // 24 KB
-constexpr uint32_t Q_CHUNK = BM * 128;            // 16 KB: 128 rows x 64 features of Q
 constexpr uint32_t V_BYTES = (DV / 64) * CHUNK_K; // 64 KB
 constexpr uint32_t P_TILE = BM * 128;             // 16 KB: 128 rows x 64 keys, bf16
 constexpr uint32_t HDR_ALPHA = P_TILE;            // float per row: O's rescale factor
@@ -180,14 +180,15 @@ struct Ctx {
 
 // ---------------------------------------------------------------- score CTA
 // The K ring carries Q too.  Ring positions count slot uses: at each segment
-// the nine 16 KB chunk images of the sequence's Q (128 rows x 64 features;
-// rows past the group read as zeros) take the next nine positions, which the
-// softmax warps move into TMEM, then every K tile takes three (its granules),
-// which the MMA warp reads.  So a segment's Q is fetched as early as the
-// ring's look-ahead allows, like a K tile.
+// the sequence's Q takes the next six positions, one box of 64 rows x 3
+// chunks each (rows 0-63 then 64-127; rows past the group read as zeros),
+// which the softmax warps move into TMEM; then every K tile takes three (its
+// granules), which the MMA warp reads.  So a segment's Q is fetched as early
+// as the ring's look-ahead allows, like a K tile, and all of it fits in the
+// ring at once.
 //
 // Warp 5: lanes 0..GRANS-1 fill the ring; lane g fills the positions
-// congruent to g mod GRANS (positions advance by 9 and 3, so a segment
+// congruent to g mod GRANS (positions advance by 6 and 3, so a segment
 // starts at a multiple of 3).  Lane kSenderLane sends each staged P block to
 // the value CTA, once the block's slot there is free, as one bulk copy that
 // completes the slot's barrier (armed by the value CTA).  Returns the number
@@ -233,15 +234,16 @@ __device__ uint32_t score_producer(const Ctx& x, const CUtensorMap* tmQ, const C
     bool ok = true;
     int ridx = 0;
     while (ok && walk.next(S)) {
-      for (int i = g; i < KCH; i += GRANS) {
+      for (int i = g; i < QPOS; i += GRANS) {
         const int idx = ridx + i;
-        if (!(ok = claim(idx, Q_CHUNK))) break;
+        if (!(ok = claim(idx, GRAN_BYTES))) break;
         const int slot = idx % KSLOTS;
-        tma_load_4d(x.sbase + OFF_K + slot * GRAN_BYTES, tmQ, x.bar(B_KFULL + slot), 0, 0, i, S.plane, pol);
+        tma_load_4d(x.sbase + OFF_K + slot * GRAN_BYTES, tmQ, x.bar(B_KFULL + slot), 0, BN * (i / GRANS),
+                    GCH * (i % GRANS), S.plane, pol);
         last = idx;
       }
       if (!ok) break;
-      ridx += KCH;
+      ridx += QPOS;
       for (int j = 0; j < S.n; ++j, ridx += GRANS) {
         const int idx = ridx + g;
         if (!(ok = claim(idx, GRAN_BYTES))) break;
@@ -283,7 +285,7 @@ __device__ void score_mma(const Ctx& x, const DecodeParams& p) {
   int c = 0, ridx = 0;
   uint32_t qph = 0;
   while (ok && walk.next(S)) {
-    ridx += KCH;   // this segment's Q chunks, which the softmax warps consume
+    ridx += QPOS;   // this segment's Q, which the softmax warps consume
     if (!(ok = warp_wait(x.bar(B_QFULL), qph, x.w))) break;
     qph ^= 1u;
     tc_fence_after();
@@ -337,30 +339,39 @@ __device__ void score_softmax(const Ctx& x, const DecodeParams& p) {
   bool ok = true;
   int c = 0, ridx = 0;
   while (ok && walk.next(S)) {
-    // Q row r of this sequence from the ring's chunk images into TMEM.  The
-    // previous segment's last score tile has been read, so every Q K^T that
-    // used the old Q has finished.  A slot goes back to the producer once all
-    // four warps have read it.
-    for (int i = 0; i < KCH; ++i) {
-      const int idx = ridx + i;
+    // Q row r of this sequence from the ring into TMEM: chunk group cg of row
+    // r is box (r / 64) * GRANS + cg, chunk cg * GCH + t at t * 8 KB and row
+    // r mod 64.  The previous segment's last score tile has been read, so
+    // every Q K^T that used the old Q has finished.  Both boxes of a chunk
+    // group go back to the producer once all four warps have read them.
+    for (int cg = 0; cg < GRANS; ++cg) {
+      const int idx = ridx + (r >> 6) * GRANS + cg;   // warp-uniform
       const int slot = idx % KSLOTS;
       const bool good = warp_wait(x.bar(B_KFULL + slot), (idx / KSLOTS) & 1, x.w);
       if (good) {
-        const uint32_t src = x.sbase + OFF_K + static_cast<uint32_t>(slot) * GRAN_BYTES + static_cast<uint32_t>(r) * 128u;
-        uint32_t w[32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          ld_shared_v4(src + ((static_cast<uint32_t>(u) ^ rsw) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-        tmem_st32u(x.tm + lane_addr + COL_Q + static_cast<uint32_t>(i) * 32u, w);
+        for (int t = 0; t < GCH; ++t) {
+          const uint32_t src = x.sbase + OFF_K + static_cast<uint32_t>(slot) * GRAN_BYTES + t * CHUNK_K +
+                               static_cast<uint32_t>(r & 63) * 128u;
+          uint32_t w[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            ld_shared_v4(src + ((static_cast<uint32_t>(u) ^ rsw) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                         w[4 * u + 3]);
+          tmem_st32u(x.tm + lane_addr + COL_Q + static_cast<uint32_t>(cg * GCH + t) * 32u, w);
+        }
       }
       if (!bar_sync_and(kQBar, 128, good)) {
         ok = false;
         break;
       }
-      if (threadIdx.x == 0) mbar_arrive(x.bar(B_KEMPTY + slot));
+      if (threadIdx.x == 0) {
+        mbar_arrive(x.bar(B_KEMPTY + (ridx + cg) % KSLOTS));
+        mbar_arrive(x.bar(B_KEMPTY + (ridx + GRANS + cg) % KSLOTS));
+      }
     }
     if (!ok) break;
-    ridx += KCH;
+    ridx += QPOS;
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
@@ -589,13 +600,13 @@ __device__ void value_rows(const Ctx& x, const DecodeParams& p) {
     // [slot][k][r]: a warp's 32 rows store 512 contiguous bytes at a time.
     float4* opart = reinterpret_cast<float4*>(p.o_part) + static_cast<size_t>(S.slot) * (DV / 4) * BM + r;
 #pragma unroll 1
-    for (int cc = 0; cc < DV / 32; ++cc) {
-      float o[32];
-      tmem_ld32(x.tm + lane_addr + COL_O + cc * 32, o);
+    for (int cc = 0; cc < DV / 64; ++cc) {
+      float o[64];
+      tmem_ld64(x.tm + lane_addr + COL_O + cc * 64, o);
       if (live) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          opart[static_cast<size_t>(cc * 8 + i) * BM] =
+        for (int i = 0; i < 16; ++i)
+          opart[static_cast<size_t>(cc * 16 + i) * BM] =
               make_float4(o[4 * i] * inv_l, o[4 * i + 1] * inv_l, o[4 * i + 2] * inv_l, o[4 * i + 3] * inv_l);
       }
     }
@@ -752,10 +763,12 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_pair_kernel(const 
     for (int i = 0; i < kCombineMaxSlots; ++i) ls[i] = (sl[i] >= 0) ? p.lse_part[sl[i] * BM + rr] : -INFINITY;
 #pragma unroll
     for (int i = 0; i < kCombineMaxSlots; ++i) mx = fmaxf(mx, ls[i]);
+    // The pieces' columns are loaded in the same round as their LSEs (a
+    // piece whose LSE is -inf holds zeros, and its weight is 0).
     float4 xv[kCombineMaxSlots][8];
 #pragma unroll
     for (int i = 0; i < kCombineMaxSlots; ++i) {
-      const bool use = ls[i] != -INFINITY;
+      const bool use = sl[i] >= 0;
       const float4* src = reinterpret_cast<const float4*>(p.o_part) + ((use ? sl[i] : 0) * (DV / 4) + blk * 8) * BM + rr;
 #pragma unroll
       for (int k = 0; k < 8; ++k) xv[i][k] = use ? src[static_cast<size_t>(k) * BM] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -814,12 +827,19 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_pair_kernel(const 
     tile[wib][lane][4 * k + 3] = acc[k].w;
   }
   __syncwarp();
-  for (int row = 0; row < 32 && r0 + row < p.group; ++row) {
-    const size_t at = out_rows + static_cast<size_t>(row) * DV + blk * 32 + lane;
+  // Four rows per store: lane l writes columns 4(l mod 8) .. +3 of row l/8.
+  const int c4 = 4 * (lane & 7);
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int row = it * 4 + (lane >> 3);
+    if (r0 + row >= p.group) continue;
+    const float a0 = tile[wib][row][c4], a1 = tile[wib][row][c4 + 1], a2 = tile[wib][row][c4 + 2],
+                a3 = tile[wib][row][c4 + 3];
+    const size_t at = out_rows + static_cast<size_t>(row) * DV + blk * 32 + c4;
     if (o != nullptr)
-      o[at] = tile[wib][row][lane];
+      *reinterpret_cast<float4*>(o + at) = make_float4(a0, a1, a2, a3);
     else
-      o_bf16[at] = static_cast<uint16_t>(pack_bf16x2(tile[wib][row][lane], 0.f) & 0xFFFFu);   // round to nearest even
+      *reinterpret_cast<uint2*>(o_bf16 + at) = make_uint2(pack_bf16x2(a0, a1), pack_bf16x2(a2, a3));
   }
   if (blk == 0 && live && lse != nullptr)
     lse[static_cast<size_t>(plane) * p.group + r] = (tot > 0.f) ? mx + logf(tot) : -INFINITY;

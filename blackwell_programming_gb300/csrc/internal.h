@@ -96,7 +96,8 @@ cudaError_t launch_latent_prefill(const LatentMaps& m, const LatentPrefillParams
 // P V.  K is read through the same 4-D view as above, in boxes of
 // kLatentKeyRows keys x kPairKeyChunks chunks (score CTA) and x
 // kPairValueChunks chunks (value CTA: V, the first 512 features), and Q in
-// boxes of 128 rows x 1 chunk (rows past the group read as zeros).  The
+// boxes of kLatentKeyRows rows x kPairKeyChunks chunks (rows past the group
+// read as zeros).  The
 // pieces go to decode_pair_slots(planes, pairs) slots of [128, 512] floats
 // and 128 LSEs, which launch_combine_pair merges.
 constexpr int kPairKeyChunks = 3;
@@ -104,7 +105,7 @@ constexpr int kPairValueChunks = 8;
 int decode_pair_slots(int planes, int pairs);
 // Clusters of the pair kernel that fit on the device at once (0 on success).
 int decode_pair_max_pairs(int num_sms, int* out);
-// `tq` maps Q [planes, group, 576] in boxes of 128 rows x 1 chunk.
+// `tq` maps Q [planes, group, 576] in boxes of 64 rows x 3 chunks.
 cudaError_t launch_decode_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                const DecodeParams& p, int pairs, cudaStream_t stream);
 cudaError_t launch_combine_pair(const DecodeParams& p, int pairs, float* o, uint16_t* o_bf16, float* lse,
