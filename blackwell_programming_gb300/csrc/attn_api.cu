@@ -207,11 +207,11 @@ int make_latent_maps(LatentMaps* m, const void* q, uint64_t q_rows, uint64_t q_p
 // The CTA-pair decode's maps: Q [planes, group, 576] in boxes of 64 rows x 3
 // chunks, and over K [planes, Nkv, 576] the score CTA's boxes of 64 keys x 3
 // chunks and the value CTA's of 64 keys x 8 chunks (V).
-int make_pair_maps(CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, const void* q, uint64_t group,
-                   const void* k, uint64_t k_rows, uint64_t planes) {
+int make_pair_maps(CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, const void* q, uint64_t q_rows,
+                   uint64_t q_planes, const void* k, uint64_t k_rows, uint64_t planes) {
   const uint64_t row = 576 * 2;
-  const uint64_t qd[4] = {64, group, 9, planes};
-  const uint64_t qs[3] = {row, 128, row * group};
+  const uint64_t qd[4] = {64, q_rows, 9, q_planes};
+  const uint64_t qs[3] = {row, 128, row * q_rows};
   const uint64_t kd[4] = {64, k_rows, 9, planes};
   const uint64_t ks[3] = {row, 128, row * k_rows};
   int st;
@@ -220,12 +220,26 @@ int make_pair_maps(CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv, const void
   return make_map4(tv, k, kd, ks, kLatentKeyRows, kPairValueChunks);
 }
 
-// Which split-KV decode kernel runs: the CTA-pair kernel (score and value
-// CTAs), or with ATTN_DECODE=single the one-CTA kernel that computes the
-// score tile in both O halves (read at every call).
-bool decode_use_pair() {
-  const char* s = std::getenv("ATTN_DECODE");
+// Which kernel runs the latent shape (decode and prefill): the CTA-pair
+// kernel (score and value CTAs), or with ATTN_LATENT=single the one-CTA
+// kernel that computes the score tile for both O halves (read at every call).
+bool latent_use_pair() {
+  const char* s = std::getenv("ATTN_LATENT");
   return !(s != nullptr && std::strcmp(s, "single") == 0);
+}
+
+// Clusters of the CTA-pair kernel that fit on the device at once (cached).
+int latent_pairs(DeviceInfo* dev, int* out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (dev->decode_pairs < 0) {
+    int n = 0;
+    const int e = decode_pair_max_pairs(dev->num_sms, &n);
+    if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "cudaOccupancyMaxActiveClusters");
+    dev->decode_pairs = n;
+  }
+  if (dev->decode_pairs <= 0) return ATTN_ERR_UNSUPPORTED;
+  *out = std::min(dev->decode_pairs, dev->num_sms / 2);
+  return ATTN_OK;
 }
 
 // Shape of one split-KV decode launch: the kernel, its CTAs (single) or
@@ -241,20 +255,13 @@ struct DecodePlan {
 
 int plan_decode(DeviceInfo* dev, int planes, int tiles, DecodePlan* out) {
   DecodePlan pl;
-  pl.pair = decode_use_pair();
+  pl.pair = latent_use_pair();
   if (pl.pair) {
-    {
-      std::lock_guard<std::mutex> lock(g_mu);
-      if (dev->decode_pairs < 0) {
-        int n = 0;
-        const int e = decode_pair_max_pairs(dev->num_sms, &n);
-        if (e != 0) return cuda_fail(static_cast<cudaError_t>(e), "cudaOccupancyMaxActiveClusters");
-        dev->decode_pairs = n;
-      }
-    }
-    if (dev->decode_pairs <= 0) return ATTN_ERR_UNSUPPORTED;
+    int pairs = 0;
+    const int st = latent_pairs(dev, &pairs);
+    if (st != ATTN_OK) return st;
     const long long total = static_cast<long long>(planes) * tiles;
-    pl.grid = static_cast<int>(std::min<long long>(total, std::min(dev->decode_pairs, dev->num_sms / 2)));
+    pl.grid = static_cast<int>(std::min<long long>(total, pairs));
     pl.rows = static_cast<size_t>(decode_pair_slots(planes, pl.grid)) * 128;
     pl.cols = 512;
   } else {
@@ -288,7 +295,7 @@ int launch_decode_plan(const DecodePlan& pl, const void* q, const void* k, float
   cudaError_t e;
   if (pl.pair) {
     CUtensorMap tq, tk, tv;
-    if ((st = make_pair_maps(&tq, &tk, &tv, q, group, k, Nkv, planes)) != ATTN_OK) return st;
+    if ((st = make_pair_maps(&tq, &tk, &tv, q, group, planes, k, Nkv, planes)) != ATTN_OK) return st;
     if ((e = launch_decode_pair(tq, tk, tv, p, pl.grid, stream)) != cudaSuccess) return cuda_fail(e, "decode launch");
     if ((e = launch_combine_pair(p, pl.grid, o32, o16, lse, stream)) != cudaSuccess)
       return cuda_fail(e, "combine launch");
@@ -490,11 +497,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint1
                           stream)) != ATTN_OK)
       return st;
   } else if (!decode) {
-    // latent shape, Nq > 1: the decode kernel in prefill mode
-    LatentMaps maps;
-    if ((st = make_latent_maps(&maps, q, Nq, static_cast<uint64_t>(B) * Hq, k, Nkv, static_cast<uint64_t>(B) * Hkv)) !=
-        ATTN_OK)
-      return st;
+    // latent shape, Nq > 1: the latent kernel in prefill mode
     LatentPrefillParams p{};
     p.q = static_cast<const uint16_t*>(q);
     p.o = o32;
@@ -508,11 +511,27 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, float* o32, uint1
     p.causal = causal ? 1 : 0;
     p.tiles = decode_tiles(Nkv);
     p.nqb = (Nq + 127) / 128;
-    p.num_units = 2 * B * Hq * p.nqb;
     p.scale_log2 = scale_log2;
     p.err = dev->err;
-    if ((e = launch_latent_prefill(maps, p, dev->num_sms, stream)) != cudaSuccess)
-      return cuda_fail(e, "latent prefill launch");
+    if (latent_use_pair()) {
+      int pairs = 0;
+      if ((st = latent_pairs(dev, &pairs)) != ATTN_OK) return st;
+      p.num_units = B * Hq * p.nqb;
+      CUtensorMap tq, tk, tv;
+      if ((st = make_pair_maps(&tq, &tk, &tv, q, Nq, static_cast<uint64_t>(B) * Hq, k, Nkv,
+                               static_cast<uint64_t>(B) * Hkv)) != ATTN_OK)
+        return st;
+      if ((e = launch_latent_prefill_pair(tq, tk, tv, p, std::min(pairs, p.num_units), stream)) != cudaSuccess)
+        return cuda_fail(e, "latent prefill launch");
+    } else {
+      LatentMaps maps;
+      if ((st = make_latent_maps(&maps, q, Nq, static_cast<uint64_t>(B) * Hq, k, Nkv,
+                                 static_cast<uint64_t>(B) * Hkv)) != ATTN_OK)
+        return st;
+      p.num_units = 2 * B * Hq * p.nqb;
+      if ((e = launch_latent_prefill(maps, p, dev->num_sms, stream)) != cudaSuccess)
+        return cuda_fail(e, "latent prefill launch");
+    }
   } else {
     const int group = Hq / Hkv;
     const int planes = B * Hkv;

@@ -35,10 +35,17 @@
 // with all SMs at once:
 //   LSE = log sum_s exp(lse_s),   O = sum_s exp(lse_s - LSE) O_s.
 //
+// Prefill (Nq > 1, causal or not): a work unit is (batch, query head, block
+// of 128 query rows) and covers every K tile the block sees -- all of them,
+// or up to the causal diagonal with bottom-right alignment -- so the value
+// CTA writes O and the score CTA the LSE directly; the same two roles, Q
+// block in the score CTA's TMEM, O in the value CTA's.
+//
 // Roles (192 threads in both CTAs): warp 5 = TMA producer, warp 4 = MMA issuer
 // (whole warp, one elected lane), warps 0-3 = one row per thread (the score
 // CTA's softmax and Q, the value CTA's rescale and epilogue).
 #include <cmath>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -141,17 +148,22 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
 
 __host__ __device__ __forceinline__ long long range_begin(long long total, int c, int n) { return total * c / n; }
 
-// One contiguous run of K tiles of one sequence inside a pair's range.
+// One run of K tiles of one sequence for one block of query rows: in decode a
+// contiguous piece of a pair's range, in prefill a whole work unit.
 struct Segment {
-  int plane;   // sequence (batch * Hkv + KV head)
-  int t0, n;   // first tile, tile count
-  int slot;    // workspace slot of its partial
+  int plane;   // K plane (batch * Hkv + KV head)
+  int qplane;  // Q plane: decode = the K plane (rows = heads), prefill = batch * Hq + head
+  int qrow0;   // first query row of the block in its Q plane
+  int t0, n;   // first tile, tile count (0: a prefill block that sees no key)
+  int slot;    // decode: workspace slot of its piece
 };
 
-struct Walker {
+// Decode: the (sequence, key tile) space cut into one contiguous equal range
+// per pair.
+struct DecodeWalker {
   long long g, g1, g0;
   int tiles, pair;
-  __device__ explicit Walker(const DecodeParams& p) {
+  __device__ explicit DecodeWalker(const DecodeParams& p) {
     const long long total = static_cast<long long>(p.planes) * p.tiles;
     pair = static_cast<int>(blockIdx.x >> 1);
     const int pairs = static_cast<int>(gridDim.x >> 1);
@@ -167,10 +179,51 @@ struct Walker {
     const long long end = min(g1, (pl + 1) * tiles);
     s.n = static_cast<int>(end - g);
     s.slot = pair + s.plane;
+    s.qplane = s.plane;
+    s.qrow0 = 0;
     g = end;
     return true;
   }
 };
+
+// Prefill: unit u = (query block counted from the bottom) * B * Hq + batch *
+// Hq + head, so long causal blocks come first and the heads that share a KV
+// head run side by side (their K tiles come from L2); the units go to the
+// pairs in rounds, every other round reversed (snake), so each pair gets a
+// similar mix of long and short blocks.
+struct PrefillWalker {
+  const LatentPrefillParams& p;
+  int it = 0;
+  __device__ explicit PrefillWalker(const LatentPrefillParams& prm) : p(prm) {}
+  __device__ bool next(Segment& s) {
+    const int pairs = static_cast<int>(gridDim.x >> 1), pair = static_cast<int>(blockIdx.x >> 1);
+    const int base = it * pairs;
+    const int u = (it & 1) ? base + pairs - 1 - pair : base + pair;
+    ++it;
+    if (u >= p.num_units) return false;
+    const int bh_count = p.B * p.Hq;
+    const int qb = p.nqb - 1 - u / bh_count;
+    const int bh = u - (u / bh_count) * bh_count;
+    const int b = bh / p.Hq, h = bh - b * p.Hq;
+    s.qplane = bh;
+    s.plane = b * p.Hkv + h / (p.Hq / p.Hkv);
+    s.qrow0 = qb * BM;
+    s.t0 = 0;
+    s.slot = 0;
+    int n = p.tiles;
+    if (p.causal) {
+      const int last_key = min(s.qrow0 + BM - 1, p.Nq - 1) + (p.Nkv - p.Nq);
+      n = last_key < 0 ? 0 : min(last_key / BN + 1, p.tiles);
+    }
+    s.n = n;
+    return true;
+  }
+};
+
+template <class P> struct WalkerFor;
+template <> struct WalkerFor<DecodeParams> { using type = DecodeWalker; };
+template <> struct WalkerFor<LatentPrefillParams> { using type = PrefillWalker; };
+template <class P> __host__ __device__ constexpr bool is_prefill() { return std::is_same<P, LatentPrefillParams>::value; }
 
 struct Ctx {
   uint32_t sbase, tm, warp, lane, peer;
@@ -193,8 +246,9 @@ struct Ctx {
 // the value CTA, once the block's slot there is free, as one bulk copy that
 // completes the slot's barrier (armed by the value CTA).  Returns the number
 // of blocks sent (on the sender lane).
-__device__ uint32_t score_producer(const Ctx& x, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                                   const DecodeParams& p) {
+template <class P>
+__device__ uint32_t score_producer(const Ctx& x, const CUtensorMap* tmQ, const CUtensorMap* tmK, const P& p) {
+  using Walker = typename WalkerFor<P>::type;
   const int g = static_cast<int>(x.lane);
   int last = -1;   // the last ring position this lane filled
   uint32_t sent = 0;
@@ -220,8 +274,9 @@ __device__ uint32_t score_producer(const Ctx& x, const CUtensorMap* tmQ, const C
       tma_prefetch_desc(tmQ);
       tma_prefetch_desc(tmK);
     }
-    // the value CTA reads the first 512 features of K again, from L2
-    const uint64_t pol = l2_policy_evict_normal();
+    // decode: the value CTA reads the first 512 features of K again, from L2;
+    // prefill: every head of the KV head and every query block reads K again
+    const uint64_t pol = is_prefill<P>() ? l2_policy_evict_last() : l2_policy_evict_normal();
     // claim ring position idx for `bytes`: wait until its slot is free
     auto claim = [&](int idx, uint32_t bytes) -> bool {
       const int slot = idx % KSLOTS;
@@ -234,12 +289,13 @@ __device__ uint32_t score_producer(const Ctx& x, const CUtensorMap* tmQ, const C
     bool ok = true;
     int ridx = 0;
     while (ok && walk.next(S)) {
+      if (S.n == 0) continue;   // a prefill block that sees no key: the row warps write it
       for (int i = g; i < QPOS; i += GRANS) {
         const int idx = ridx + i;
         if (!(ok = claim(idx, GRAN_BYTES))) break;
         const int slot = idx % KSLOTS;
-        tma_load_4d(x.sbase + OFF_K + slot * GRAN_BYTES, tmQ, x.bar(B_KFULL + slot), 0, BN * (i / GRANS),
-                    GCH * (i % GRANS), S.plane, pol);
+        tma_load_4d(x.sbase + OFF_K + slot * GRAN_BYTES, tmQ, x.bar(B_KFULL + slot), 0, S.qrow0 + BN * (i / GRANS),
+                    GCH * (i % GRANS), S.qplane, pol);
         last = idx;
       }
       if (!ok) break;
@@ -277,7 +333,9 @@ __device__ uint32_t score_producer(const Ctx& x, const CUtensorMap* tmQ, const C
 
 // Warp 4: S = Q K^T (36 MMAs of 16 features, A = Q in TMEM) into score
 // buffer c & 1, once the softmax has read what the buffer held two tiles ago.
-__device__ void score_mma(const Ctx& x, const DecodeParams& p) {
+template <class P>
+__device__ void score_mma(const Ctx& x, const P& p) {
+  using Walker = typename WalkerFor<P>::type;
   const uint64_t kd0 = smem_desc_sw128(x.sbase + OFF_K, 16, 1024);
   Walker walk(p);
   Segment S;
@@ -285,6 +343,7 @@ __device__ void score_mma(const Ctx& x, const DecodeParams& p) {
   int c = 0, ridx = 0;
   uint32_t qph = 0;
   while (ok && walk.next(S)) {
+    if (S.n == 0) continue;
     ridx += QPOS;   // this segment's Q, which the softmax warps consume
     if (!(ok = warp_wait(x.bar(B_QFULL), qph, x.w))) break;
     qph ^= 1u;
@@ -328,7 +387,9 @@ __device__ void score_mma(const Ctx& x, const DecodeParams& p) {
 // copies to the value CTA.  Each warp runs on its own: it waits for the
 // staging buffer's previous copy to have landed, writes its 32 rows and
 // arrives on the buffer's barrier.
-__device__ void score_softmax(const Ctx& x, const DecodeParams& p) {
+template <class P>
+__device__ void score_softmax(const Ctx& x, const P& p) {
+  using Walker = typename WalkerFor<P>::type;
   const int r = static_cast<int>(x.warp * 32 + x.lane);
   const uint32_t lane_addr = (x.warp * 32u) << 16;
   const float sl2 = p.scale_log2;
@@ -339,6 +400,22 @@ __device__ void score_softmax(const Ctx& x, const DecodeParams& p) {
   bool ok = true;
   int c = 0, ridx = 0;
   while (ok && walk.next(S)) {
+    bool live = true;
+    // The last key row r may see (all of them, or up to the causal diagonal
+    // with bottom-right alignment), and the first row's limit: a tile whose
+    // last key is past it needs the mask.
+    int key_lim = p.Nkv - 1, lim0 = p.Nkv - 1;
+    if constexpr (is_prefill<P>()) {
+      live = S.qrow0 + r < p.Nq;
+      if (p.causal) {
+        key_lim = min(S.qrow0 + r + (p.Nkv - p.Nq), p.Nkv - 1);
+        lim0 = S.qrow0 + (p.Nkv - p.Nq);
+      }
+      if (S.n == 0) {   // a block that sees no key
+        if (live && p.lse != nullptr) p.lse[static_cast<size_t>(S.qplane) * p.Nq + S.qrow0 + r] = -INFINITY;
+        continue;
+      }
+    }
     // Q row r of this sequence from the ring into TMEM: chunk group cg of row
     // r is box (r / 64) * GRANS + cg, chunk cg * GCH + t at t * 8 KB and row
     // r mod 64.  The previous segment's last score tile has been read, so
@@ -388,11 +465,11 @@ __device__ void score_softmax(const Ctx& x, const DecodeParams& p) {
       __syncwarp();
       if (x.lane == 0) mbar_arrive(x.bar(B_SFREE + b));
       const int key0 = (S.t0 + j) * BN;
-      const bool ragged = key0 + BN > p.Nkv;
+      const bool ragged = key0 + BN - 1 > lim0;
       if (ragged) {
 #pragma unroll
         for (int i = 0; i < BN; ++i)
-          if (key0 + i >= p.Nkv) v[i] = -INFINITY;
+          if (key0 + i > key_lim) v[i] = -INFINITY;
       }
       float mx8[8];
 #pragma unroll
@@ -441,8 +518,12 @@ __device__ void score_softmax(const Ctx& x, const DecodeParams& p) {
                      pk[4 * u + 3]);
       st_shared_f32(stg + HDR_ALPHA + 4u * r, alpha);
       if (j == S.n - 1) {
+        const float lse_r = l > 0.f ? (R + __log2f(l)) * 0.69314718055994531f : -INFINITY;
         st_shared_f32(stg + HDR_INVL + 4u * r, l > 0.f ? 1.f / l : 0.f);
-        st_shared_f32(stg + HDR_LSE + 4u * r, l > 0.f ? (R + __log2f(l)) * 0.69314718055994531f : -INFINITY);
+        st_shared_f32(stg + HDR_LSE + 4u * r, lse_r);
+        if constexpr (is_prefill<P>()) {
+          if (live && p.lse != nullptr) p.lse[static_cast<size_t>(S.qplane) * p.Nq + S.qrow0 + r] = lse_r;
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -457,7 +538,9 @@ __device__ void score_softmax(const Ctx& x, const DecodeParams& p) {
 // Lane 1: as each P block lands, tells the score CTA that the staging buffer
 // it came from may be refilled (the row warps cannot, as they are busy during
 // an epilogue).
-__device__ void value_producer(const Ctx& x, const CUtensorMap* tmV, const DecodeParams& p) {
+template <class P>
+__device__ void value_producer(const Ctx& x, const CUtensorMap* tmV, const P& p) {
+  using Walker = typename WalkerFor<P>::type;
   if (x.lane == 1) {
     const uint32_t stgfree_peer = mapa_shared(x.bar(B_STGFREE), x.peer);
     Walker walk(p);
@@ -472,7 +555,8 @@ __device__ void value_producer(const Ctx& x, const CUtensorMap* tmV, const Decod
     }
   } else if (x.lane == 0) {
     tma_prefetch_desc(tmV);
-    const uint64_t pol = l2_policy_evict_first();   // the score CTA has read this tile already
+    // decode: the score CTA has read this tile already; prefill: other blocks read it again
+    const uint64_t pol = is_prefill<P>() ? l2_policy_evict_last() : l2_policy_evict_first();
     Walker walk(p);
     Segment S;
     bool ok = true;
@@ -500,7 +584,9 @@ __device__ void value_producer(const Ctx& x, const CUtensorMap* tmV, const Decod
 // in the score CTA's flow control (a commit that arrives there by offset).
 // The row warps read the block's header before they arrive on B_CORR, which
 // this warp waits for before the P V, so the commit also covers those reads.
-__device__ void value_mma(const Ctx& x, const DecodeParams& p) {
+template <class P>
+__device__ void value_mma(const Ctx& x, const P& p) {
+  using Walker = typename WalkerFor<P>::type;
   const uint64_t pd0 = smem_desc_sw128(x.sbase + OFF_P, 16, 1024);
   const uint64_t vd0 = smem_desc_sw128(x.sbase + OFF_V, CHUNK_K, 1024);
   const uint16_t peer_mask = static_cast<uint16_t>(1u << x.peer);
@@ -545,21 +631,79 @@ __device__ void value_mma(const Ctx& x, const DecodeParams& p) {
   __syncwarp();
 }
 
+// Prefill: the block's O rows straight to the output, normalised.  O leaves
+// TMEM in the 16x256b shape (lane i holds columns 8k + 2(i mod 4), +1 of rows
+// i/4 and i/4 + 8 of a 16-row group), so each warp store writes 8 rows x 32
+// contiguous bytes.
+__device__ void write_block(const Ctx& x, const LatentPrefillParams& p, const Segment& S, float inv_l) {
+  const int lane = static_cast<int>(x.lane);
+  const bool bf = p.o == nullptr;
+#pragma unroll 1
+  for (int hl = 0; hl < 2; ++hl) {
+    const int src = hl * 16 + (lane >> 2);   // the lanes that own rows ra and ra + 8 above
+    const int ra = static_cast<int>(x.warp) * 32 + src;
+    const float iA = __shfl_sync(kFull, inv_l, src), iB = __shfl_sync(kFull, inv_l, src + 8);
+    const bool lA = S.qrow0 + ra < p.Nq, lB = S.qrow0 + ra + 8 < p.Nq;
+    const size_t base = static_cast<size_t>(S.qplane) * p.Nq + S.qrow0;
+    const size_t oA = (base + (lA ? ra : 0)) * DV + 2 * (lane & 3);
+    const size_t oB = (base + (lB ? ra + 8 : 0)) * DV + 2 * (lane & 3);
+#pragma unroll 1
+    for (int ch = 0; ch < DV / 64; ++ch) {
+      uint32_t v[32];
+      tmem_ld16x256b_x8(x.tm + ((x.warp * 32u + static_cast<uint32_t>(hl) * 16u) << 16) + COL_O + ch * 64, v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const size_t col = static_cast<size_t>(ch * 64 + 8 * k);
+        const float a0 = __uint_as_float(v[4 * k]) * iA, a1 = __uint_as_float(v[4 * k + 1]) * iA;
+        const float b0 = __uint_as_float(v[4 * k + 2]) * iB, b1 = __uint_as_float(v[4 * k + 3]) * iB;
+        if (bf) {
+          if (lA) *reinterpret_cast<uint32_t*>(p.o_bf16 + oA + col) = pack_bf16x2(a0, a1);
+          if (lB) *reinterpret_cast<uint32_t*>(p.o_bf16 + oB + col) = pack_bf16x2(b0, b1);
+        } else {
+          if (lA) *reinterpret_cast<float2*>(p.o + oA + col) = make_float2(a0, a1);
+          if (lB) *reinterpret_cast<float2*>(p.o + oB + col) = make_float2(b0, b1);
+        }
+      }
+    }
+  }
+}
+
 // Warps 0-3: per tile, the row's rescale factor from the block header (O is
 // rescaled, after the previous tile's P V, when any row of the warp grew its
 // reference); warp 0 then arms the slot's barrier for the block that will
-// land there next.  At a segment's end the normalised piece and its LSE go
-// to the segment's workspace slot.
-__device__ void value_rows(const Ctx& x, const DecodeParams& p) {
+// land there next.  At a segment's end the normalised O goes to the output
+// (prefill) or, as a piece with its LSE, to the segment's workspace slot
+// (decode).
+template <class P>
+__device__ void value_rows(const Ctx& x, const P& p) {
+  using Walker = typename WalkerFor<P>::type;
   const int r = static_cast<int>(x.warp * 32 + x.lane);
   const uint32_t lane_addr = (x.warp * 32u) << 16;
-  const bool live = r < p.group;
   Walker walk(p);
   Segment S;
   bool ok = true;
   int c = 0;
   uint32_t ofph = 0;
   while (ok && walk.next(S)) {
+    bool live;
+    if constexpr (is_prefill<P>()) {
+      live = S.qrow0 + r < p.Nq;
+      if (S.n == 0) {   // a block that sees no key: O = 0
+        if (live) {
+          const size_t orow = (static_cast<size_t>(S.qplane) * p.Nq + S.qrow0 + r) * DV;
+          if (p.o != nullptr) {
+#pragma unroll 4
+            for (int k = 0; k < DV / 4; ++k) reinterpret_cast<float4*>(p.o + orow)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          } else {
+#pragma unroll 4
+            for (int k = 0; k < DV / 8; ++k) reinterpret_cast<uint4*>(p.o_bf16 + orow)[k] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        continue;
+      }
+    } else {
+      live = r < p.group;
+    }
     float inv_l = 0.f, lse_own = -INFINITY;
     for (int j = 0; j < S.n; ++j, ++c) {
       const int s = c % NP;
@@ -596,30 +740,35 @@ __device__ void value_rows(const Ctx& x, const DecodeParams& p) {
     if (!(ok = warp_wait(x.bar(B_OFULL), ofph, x.w))) break;
     ofph ^= 1u;
     tc_fence_after();
-    // Normalised piece, with the float4 of row r and columns 4k..4k+3 at
-    // [slot][k][r]: a warp's 32 rows store 512 contiguous bytes at a time.
-    float4* opart = reinterpret_cast<float4*>(p.o_part) + static_cast<size_t>(S.slot) * (DV / 4) * BM + r;
-#pragma unroll 1
-    for (int cc = 0; cc < DV / 64; ++cc) {
-      float o[64];
-      tmem_ld64(x.tm + lane_addr + COL_O + cc * 64, o);
-      if (live) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          opart[static_cast<size_t>(cc * 16 + i) * BM] =
-              make_float4(o[4 * i] * inv_l, o[4 * i + 1] * inv_l, o[4 * i + 2] * inv_l, o[4 * i + 3] * inv_l);
+    if constexpr (is_prefill<P>()) {
+      write_block(x, p, S, inv_l);
+    } else {
+      // Normalised piece, with the float4 of row r and columns 4k..4k+3 at
+      // [slot][k][r]: a warp's 32 rows store 512 contiguous bytes at a time.
+      float4* opart = reinterpret_cast<float4*>(p.o_part) + static_cast<size_t>(S.slot) * (DV / 4) * BM + r;
+  #pragma unroll 1
+      for (int cc = 0; cc < DV / 64; ++cc) {
+        float o[64];
+        tmem_ld64(x.tm + lane_addr + COL_O + cc * 64, o);
+        if (live) {
+  #pragma unroll
+          for (int i = 0; i < 16; ++i)
+            opart[static_cast<size_t>(cc * 16 + i) * BM] =
+                make_float4(o[4 * i] * inv_l, o[4 * i + 1] * inv_l, o[4 * i + 2] * inv_l, o[4 * i + 3] * inv_l);
+        }
       }
+      if (live) p.lse_part[static_cast<size_t>(S.slot) * BM + r] = lse_own;
     }
-    if (live) p.lse_part[static_cast<size_t>(S.slot) * BM + r] = lse_own;
     tc_fence_before();
     __syncwarp();
     if (x.lane == 0) mbar_arrive(x.bar(B_OEMPTY));
   }
 }
 
+template <class P>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     latent_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const DecodeParams p) {
+                       const __grid_constant__ CUtensorMap tmV, const P p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctx x;
@@ -850,7 +999,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_pair_kernel(const 
 int decode_pair_slots(int planes, int pairs) { return pairs + planes - 1; }
 
 int decode_pair_max_pairs(int num_sms, int* out) {
-  cudaError_t e = cudaFuncSetAttribute(latent_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // Both instances (decode and prefill) use the same resources.
+  cudaError_t e = cudaFuncSetAttribute(latent_pair_kernel<DecodeParams>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return static_cast<int>(e);
   cudaLaunchConfig_t cfg = {};
@@ -865,18 +1015,31 @@ int decode_pair_max_pairs(int num_sms, int* out) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if ((e = cudaOccupancyMaxActiveClusters(&n, latent_pair_kernel, &cfg)) != cudaSuccess) return static_cast<int>(e);
+  if ((e = cudaOccupancyMaxActiveClusters(&n, latent_pair_kernel<DecodeParams>, &cfg)) != cudaSuccess)
+    return static_cast<int>(e);
   *out = n;
   return 0;
 }
 
-cudaError_t launch_decode_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                               const DecodeParams& p, int pairs, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(latent_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <class P>
+cudaError_t launch_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const P& p, int pairs,
+                        cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(latent_pair_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  latent_pair_kernel<<<2 * pairs, kThreads, SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  if (pairs <= 0) return cudaSuccess;
+  latent_pair_kernel<P><<<2 * pairs, kThreads, SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_decode_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                               const DecodeParams& p, int pairs, cudaStream_t stream) {
+  return launch_pair(tq, tk, tv, p, pairs, stream);
+}
+
+cudaError_t launch_latent_prefill_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                       const LatentPrefillParams& p, int pairs, cudaStream_t stream) {
+  return launch_pair(tq, tk, tv, p, pairs, stream);
 }
 
 cudaError_t launch_combine_pair(const DecodeParams& p, int pairs, float* o, uint16_t* o_bf16, float* lse,

@@ -110,6 +110,10 @@ cudaError_t launch_decode_pair(const CUtensorMap& tq, const CUtensorMap& tk, con
                                const DecodeParams& p, int pairs, cudaStream_t stream);
 cudaError_t launch_combine_pair(const DecodeParams& p, int pairs, float* o, uint16_t* o_bf16, float* lse,
                                 cudaStream_t stream);
+// The latent prefill on the same CTA pairs (num_units = B * Hq * nqb), with
+// Q mapped as [B * Hq, Nq, 576] and K as [B * Hkv, Nkv, 576] like the decode.
+cudaError_t launch_latent_prefill_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                       const LatentPrefillParams& p, int pairs, cudaStream_t stream);
 
 // Number of partial slots each CTA needs for a grid of `grid` CTAs.
 int decode_max_segments(int planes, int tiles, int grid);

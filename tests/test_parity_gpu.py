@@ -94,14 +94,14 @@ SMALL = [
       scale=1 / math.sqrt(192), v_aliases_k=True),
 ]
 
-DECODE = [w for w in SMALL if w.d_qk == 576 and w.Nq == 1 and w.Hq // w.Hkv <= 128]
+LATENT = [w for w in SMALL if w.d_qk == 576]
 
 
-@pytest.mark.parametrize("wl", DECODE, ids=lambda w: w.name)
-def test_decode_one_cta_kernel_full_parity(wl, monkeypatch):
-    """The one-CTA decode kernel (ATTN_DECODE=single), kept for comparison,
+@pytest.mark.parametrize("wl", LATENT, ids=lambda w: w.name)
+def test_latent_one_cta_kernel_full_parity(wl, monkeypatch):
+    """The one-CTA latent kernel (ATTN_LATENT=single), kept for comparison,
     meets the same parity bar as the default CTA-pair kernel."""
-    monkeypatch.setenv("ATTN_DECODE", "single")
+    monkeypatch.setenv("ATTN_LATENT", "single")
     full_case(wl)
 
 
