@@ -39,8 +39,8 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {"gemm": "blackwell_programming_gb300/csrc/gemm_sm103.cu",
                   "prefill": "blackwell_programming_gb300/csrc/prefill_sm103.cu",
-                  "decode": "blackwell_programming_gb300/csrc/decode_sm103.cu",
-                  "latent_prefill": "blackwell_programming_gb300/csrc/decode_sm103.cu"}
+                  "decode": "blackwell_programming_gb300/csrc/decode_pair_sm103.cu",
+                  "latent_prefill": "blackwell_programming_gb300/csrc/decode_pair_sm103.cu"}
 
 
 # ----------------------------------------------------------------- helpers
@@ -445,7 +445,7 @@ def roofline_for(wl, per_launch: float, peaks, peak_src: str):
     kind = ("decode" if wl.Nq == 1 else "latent_prefill") if wl.d_qk == 576 else "prefill"
     if kind in ("prefill", "latent_prefill"):
         achieved = flops / per_launch / 1e12
-        kname = {64: "prefill_kernel<64>", 128: "prefill_kernel<128>"}.get(wl.d_qk, "latent_kernel (prefill mode)")
+        kname = {64: "prefill_kernel<64>", 128: "prefill_kernel<128>"}.get(wl.d_qk, "latent_pair_kernel (prefill mode)")
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16_tflops"], "peak_source": peak_src + " bf16_tflops (burst)",
                 "kernel": kname, "algorithmic_flops_per_launch": flops}
@@ -453,7 +453,7 @@ def roofline_for(wl, per_launch: float, peaks, peak_src: str):
         achieved = algorithmic_bytes(wl) / per_launch / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peak_src + " hbm_gbs",
-                "kernel": "latent_kernel (decode mode) + combine_kernel (one step)",
+                "kernel": "latent_pair_kernel (decode mode) + combine_pair_kernel (one step)",
                 "algorithmic_bytes_per_launch": algorithmic_bytes(wl),
                 "tensor_tflops": flops / per_launch / 1e12}
     traffic_key = wl.name + ("_dropout%g" % DROPOUT if DROPOUT > 0.0 else "")
