@@ -167,6 +167,25 @@ int make_map4(CUtensorMap* m, const void* base, const uint64_t dims[4], const ui
   return ATTN_OK;
 }
 
+// C [M, N] (bf16 or fp32) as a 2-D map with boxes of 32 rows x 128 bytes
+// and the 128-byte swizzle: the GEMM's TMA-store epilogue.
+int make_c_map(CUtensorMap* m, void* c, int M, int N, bool fp32) {
+  const uint64_t es = fp32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {es * static_cast<uint64_t>(N)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / es), 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(t_cuda_error, sizeof(t_cuda_error), "cuTensorMapEncodeTiled (C) failed (CUresult %d)",
+                  static_cast<int>(r));
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
 // Map of one prefill operand with H heads of N rows of d features per batch.
 // Head-major [B, H, N, d] (ld == 0): dimensions (d, N, H, B), 128-row boxes
 // along N.  Token-major (ld > 0 = elements from one token's row to the
@@ -596,9 +615,17 @@ int gemm_bf16_nt(const void* a, const void* b, void* c, int M, int N, int K, int
     p.group_m = (g >= 1 && g <= 1024) ? g : kGemmGroupM;
   }
   p.err = dev->err;
+  // The pair kernel writes C with TMA stores when C's row pitch is a
+  // multiple of 16 bytes (ATTN_GEMM_DIRECT_STORE=1 keeps the register stores).
+  CUtensorMap tc;
+  const CUtensorMap* ptc = nullptr;
+  if (use_pair && N % 8 == 0 && !env_flag("ATTN_GEMM_DIRECT_STORE")) {
+    if ((st = make_c_map(&tc, c, M, N, c_fp32 != 0)) != ATTN_OK) return st;
+    ptc = &tc;
+  }
   cudaError_t e;
-  if ((e = use_pair ? launch_gemm_pair(ta, tb, p, dev->num_sms, stream) : launch_gemm(ta, tb, p, dev->num_sms, stream)) !=
-      cudaSuccess)
+  if ((e = use_pair ? launch_gemm_pair(ta, tb, ptc, p, dev->num_sms, stream)
+                    : launch_gemm(ta, tb, p, dev->num_sms, stream)) != cudaSuccess)
     return cuda_fail(e, "gemm launch");
   if (check_env()) return read_device_error(stream, dev->err, 0);
   return ATTN_OK;

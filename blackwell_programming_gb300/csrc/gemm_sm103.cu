@@ -233,7 +233,11 @@ constexpr int kStages = 6;
 constexpr uint32_t A_BYTES = BM * BK * 2;    // 16 KB
 constexpr uint32_t B_BYTES = BNH * BK * 2;   // 16 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t OFF_BAR = kStages * STAGE_BYTES;
+// TMA-store epilogue staging: per epilogue warp two 4 KB buffers of 32 rows x
+// 128 bytes (a box of 64 bf16 or 32 fp32 columns, 128-byte swizzle).
+constexpr uint32_t OUT_WARP_BYTES = 32 * 128;
+constexpr uint32_t OFF_OUT = kStages * STAGE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_OUT + 4 * 2 * OUT_WARP_BYTES;
 constexpr int B_FULL = 0, B_EMPTY = kStages, B_ACCFULL = 2 * kStages, B_ACCEMPTY = B_ACCFULL + 2,
               B_DRAIN = B_ACCEMPTY + 2, NUM_BARS = B_DRAIN + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -261,9 +265,13 @@ __device__ __forceinline__ bool warp_wait_cl(uint32_t bar, uint32_t parity, cons
 
 }  // namespace pair
 
+// TMA_STORE: the epilogue stages each 32-row x 128-byte block of C in shared
+// memory and writes it with a TMA store (C's row pitch a multiple of 16
+// bytes); otherwise it stores straight from registers.
+template <bool TMA_STORE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const GemmParams p) {
+                     const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   // the pair's tile shape and layout (shadowing the single-CTA constants)
   constexpr int BM = pair::BM, BN = pair::BN, BNH = pair::BNH, kStages = pair::kStages;
   constexpr uint32_t A_BYTES = pair::A_BYTES, STAGE_BYTES = pair::STAGE_BYTES, OFF_BAR = pair::OFF_BAR,
@@ -379,6 +387,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t afph = 0u;
     bool ok = true;
     int i = 0;
+    int nstore = 0;   // TMA stores this warp has issued (lane 0)
     for (int t = cid; t < p.num_tiles && ok; t += ncl, ++i) {
       const int a = i & 1;
       int mb, nb;
@@ -386,8 +395,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!(ok = warp_wait_cl(bar(B_ACCFULL + a), (afph >> a) & 1u, wctx))) break;
       afph ^= 1u << a;
       tc_fence_after();
-      const int col0 = nb * BN + 2 * static_cast<int>(lane & 3);
       const int row0 = mb * 2 * BM + static_cast<int>(rank) * BM;
+      if constexpr (TMA_STORE) {
+        // Row `lane` of this warp's 32 rows, one 128-byte block of C at a
+        // time: TMEM -> registers -> a swizzled staging buffer -> one TMA
+        // store of 32 rows.  Two buffers per warp; a buffer is rewritten
+        // once the store issued from it two blocks ago has read it.
+        const int cols = p.c_fp32 ? 32 : 64;   // columns per 128-byte block
+        const uint32_t rsw = lane & 7u;
+        const uint32_t stage0 = sbase + pair::OFF_OUT + quad * 2u * pair::OUT_WARP_BYTES;
+#pragma unroll 1
+        for (int blk = 0; blk < BN / cols; ++blk, ++nstore) {
+          const uint32_t buf = stage0 + static_cast<uint32_t>(nstore & 1) * pair::OUT_WARP_BYTES;
+          uint32_t w[32];
+          if (p.c_fp32) {
+            float v[32];
+            tmem_ld32(tm + ((quad * 32u) << 16) + a * BN + blk * 32, v);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) w[k] = __float_as_uint(v[k]);
+          } else {
+            float v[32], u[32];
+            tmem_ld32(tm + ((quad * 32u) << 16) + a * BN + blk * 64, v);
+            tmem_ld32(tm + ((quad * 32u) << 16) + a * BN + blk * 64 + 32, u);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+              w[16 + k] = pack_bf16x2(u[2 * k], u[2 * k + 1]);
+            }
+          }
+          if (nstore >= 2) {
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            st_shared_v4(buf + lane * 128u + ((static_cast<uint32_t>(u) ^ rsw) << 4), w[4 * u], w[4 * u + 1],
+                         w[4 * u + 2], w[4 * u + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, buf, nb * BN + blk * cols, row0 + static_cast<int>(quad) * 32);
+            bulk_commit_group();
+          }
+        }
+        // the accumulator is in the staging buffers (or already written)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(bar(B_ACCEMPTY + a), 0));
+        continue;
+      }
+      const int col0 = nb * BN + 2 * static_cast<int>(lane & 3);
 #pragma unroll 1
       for (int hl = 0; hl < 2; ++hl) {
         const int ra = row0 + static_cast<int>(quad * 32 + hl * 16 + (lane >> 2));
@@ -418,6 +475,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(bar(B_ACCEMPTY + a), 0));
     }
+    // every store has written global memory before the CTA exits
+    if (TMA_STORE && lane == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -437,14 +497,23 @@ int gemm_tile_depth() { return BK; }
 bool gemm_use_pair(int M) { return M > BM; }
 int gemm_b_box_rows(bool use_pair) { return use_pair ? pair::BNH : BN; }
 
-cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int num_sms,
-                             cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(pair::SMEM_BYTES));
-  if (e != cudaSuccess) return e;
+cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tc,
+                             const GemmParams& p, int num_sms, cudaStream_t stream) {
   const int clusters = min(p.num_tiles, num_sms / 2);
-  if (clusters <= 0) return cudaSuccess;
-  gemm_pair_kernel<<<2 * clusters, kThreads, pair::SMEM_BYTES, stream>>>(ta, tb, p);
+  cudaError_t e;
+  if (tc != nullptr) {
+    if ((e = cudaFuncSetAttribute(gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(pair::SMEM_BYTES))) != cudaSuccess)
+      return e;
+    if (clusters <= 0) return cudaSuccess;
+    gemm_pair_kernel<true><<<2 * clusters, kThreads, pair::SMEM_BYTES, stream>>>(ta, tb, *tc, p);
+  } else {
+    if ((e = cudaFuncSetAttribute(gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(pair::SMEM_BYTES))) != cudaSuccess)
+      return e;
+    if (clusters <= 0) return cudaSuccess;
+    gemm_pair_kernel<false><<<2 * clusters, kThreads, pair::SMEM_BYTES, stream>>>(ta, tb, ta, p);
+  }
   return cudaGetLastError();
 }
 

@@ -146,8 +146,11 @@ int gemm_tile_depth();
 // blocks.
 bool gemm_use_pair(int M);
 int gemm_b_box_rows(bool use_pair);
-cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int num_sms,
-                             cudaStream_t stream);
+// `tc` (or null): C as a 2-D map (N, M) with boxes of 32 rows x 128 bytes and
+// the 128-byte swizzle, for the TMA-store epilogue (C's row pitch a multiple
+// of 16 bytes); null: the epilogue stores from registers.
+cudaError_t launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap* tc,
+                             const GemmParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int num_sms,
                         cudaStream_t stream);
 

@@ -6,9 +6,10 @@ serving loop with a fixed memory budget, a plug-in whose host forbids
 allocation).  For them the library's split-KV decode has a variant whose
 partial results live in a fixed static device array instead of a
 stream-ordered pool workspace.  These checks call it through the C ABI and hold
-its output to the same tolerance as every other parity test, against the
-regular attn_fwd path, on two calls in a row (the array keeps the previous
-call's contents, so the second call must not depend on it being clear).
+its output to the same tolerance as every other parity test, against the fp64
+oracle and against the regular attn_fwd path on two calls in a row (the array
+keeps the previous call's contents, so the second call must not depend on it
+being clear).
 
 The file is named to be collected last, so a failure here leaves every other
 test already run.
@@ -61,6 +62,28 @@ def test_noalloc_matches_attn_fwd_twice(gb, B, Hq, Hkv, Nkv):
         assert gb.attn_check_device(reset=True) == 0
         assert torch.isfinite(o).all() and torch.isfinite(lse).all(), call
         _close(o, lse, o_ref, l_ref)
+
+
+def test_noalloc_matches_the_oracle(gb):
+    """attn_decode_fwd_noalloc against the fp64 oracle directly, element by
+    element, on a case whose rows merge several split pieces."""
+    from oracle import attention
+    wl = syn.Workload("noalloc_oracle", 2, 32, 1, 1, 700, 576, 512, False, 1 / math.sqrt(192), v_aliases_k=True)
+    inp = syn.make_inputs(wl)
+    q, k, _ = to_torch(inp)
+    o = torch.full((wl.B, wl.Hq, 1, 512), float("nan"), device="cuda")
+    lse = torch.full((wl.B, wl.Hq, 1), float("nan"), device="cuda")
+    st = gb.attn_decode_fwd_noalloc(q.data_ptr(), k.data_ptr(), o.data_ptr(), lse.data_ptr(), wl.B, wl.Hq, wl.Hkv,
+                                    wl.Nkv, wl.scale, torch.cuda.current_stream().cuda_stream)
+    assert st == gb.ATTN_OK, (gb.attn_status_string(st), gb.attn_last_cuda_error())
+    torch.cuda.synchronize()
+    assert gb.attn_check_device(reset=True) == 0
+    qf, kf, vf = inp.f64()
+    o_ref, lse_ref = attention(qf, kf, vf, False, wl.scale)
+    d = np.abs(o.cpu().numpy() - o_ref)
+    assert float(d.max()) <= O_MAX_ABS and float(d.mean()) <= O_MEAN_ABS
+    rel = np.abs(lse.cpu().numpy() - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
+    assert float(rel.max()) <= LSE_REL
 
 
 def test_noalloc_rejects_problems_beyond_the_static_scratch(gb):
