@@ -781,6 +781,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC + 4);
   volatile uint32_t* sent_count = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC + 8);
   x.w = WaitCtx{abort_flag, p.err};
+  // The merge kernel that follows a decode launch may be scheduled now: its
+  // blocks wait for this grid to complete before they read anything.
+  grid_launch_dependents();
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
@@ -875,6 +878,9 @@ constexpr int kCombineMaxSlots = 4;   // pieces per sequence handled in register
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_pair_kernel(const DecodeParams p, int pairs, float* o,
                                                                           uint16_t* o_bf16, float* lse) {
   __shared__ float tile[kCombineWarps][32][33];
+  // launched as a programmatic dependent of the decode grid: its pieces are
+  // read only once that grid has completed
+  grid_dependency_wait();
   const int wib = static_cast<int>(threadIdx.x >> 5);
   const int wid = blockIdx.x * kCombineWarps + wib;
   const int lane = static_cast<int>(threadIdx.x & 31);
@@ -1045,9 +1051,19 @@ cudaError_t launch_latent_prefill_pair(const CUtensorMap& tq, const CUtensorMap&
 cudaError_t launch_combine_pair(const DecodeParams& p, int pairs, float* o, uint16_t* o_bf16, float* lse,
                                 cudaStream_t stream) {
   const int warps = p.planes * ((p.group + 31) / 32) * (DV / 32);
-  combine_pair_kernel<<<(warps + kCombineWarps - 1) / kCombineWarps, kCombineWarps * 32, 0, stream>>>(p, pairs, o,
-                                                                                                      o_bf16, lse);
-  return cudaGetLastError();
+  // Programmatic stream serialization: the merge grid is set up while the
+  // decode grid runs and starts as soon as that grid has completed.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((warps + kCombineWarps - 1) / kCombineWarps), 1u, 1u);
+  cfg.blockDim = dim3(kCombineWarps * 32, 1u, 1u);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_pair_kernel, p, pairs, o, o_bf16, lse);
 }
 
 }  // namespace gbattn
