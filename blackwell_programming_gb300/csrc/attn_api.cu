@@ -344,6 +344,13 @@ int exp2_split() {
   return (v == 4 || v == 8) ? v : 0;
 }
 
+// Key-split units for problems under one wave (d = 64): on unless
+// ATTN_PREFILL_KVSPLIT=0 (read at every call).
+bool prefill_kv_split_enabled() {
+  const char* s = std::getenv("ATTN_PREFILL_KVSPLIT");
+  return s == nullptr || s[0] != '0';
+}
+
 bool check_env() {
   static const bool on = [] {
     const char* s = std::getenv("ATTN_CHECK");
@@ -462,6 +469,10 @@ int run_prefill(const void* q, const void* k, const void* v, float* o32, uint16_
   // Two 128-row tiles per unit (they ping-pong on the tensor core); one when
   // two-tile units would leave SMs idle, so that more SMs share the work.
   p.tiles_per_unit = (static_cast<long long>(B) * Hq * ((Nq + 255) / 256) < dev->num_sms) ? 1 : 2;
+  // With one tile per unit the second tile slot would idle: at d = 64 it
+  // takes the second half of the unit's key tiles instead (the merge buffer
+  // fits beside the d = 64 rings only).
+  p.kv_split = (p.tiles_per_unit == 1 && d == 64 && prefill_kv_split_enabled()) ? 1 : 0;
   p.nqb = (Nq + 128 * p.tiles_per_unit - 1) / (128 * p.tiles_per_unit);
   p.nkv_tiles = (Nkv + 127) / 128;
   p.num_units = B * Hq * p.nqb;

@@ -34,6 +34,10 @@ struct PrefillParams {
   // 0 = all on the SFU), dropout-free kernels only.
   int exp2_split;
   int tiles_per_unit;  // 128-row query tiles per work unit: 2, or 1 for problems under one wave
+  // 1: a unit is one 128-row query tile and both tile slots take it, slot 0
+  // the first ceil(n / 2) of its n key tiles and slot 1 the rest; the two
+  // partial softmax states are merged in the epilogue (tiles_per_unit 1, D 64)
+  int kv_split;
   int num_units;       // B * Hq * nqb
   int nqb;             // ceil(Nq / (128 * tiles_per_unit))
   int nkv_tiles;       // ceil(Nkv / 128)

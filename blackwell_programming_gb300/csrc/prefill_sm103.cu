@@ -73,9 +73,13 @@ struct Cfg {
   static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KFULL = 4, B_KEMPTY = 4 + KS, B_VFULL = 4 + 2 * KS,
                        B_VEMPTY = 4 + 2 * KS + VS, B_SFULL = 4 + 2 * KS + 2 * VS, B_PFULL = B_SFULL + 2,
                        B_OFULL = B_PFULL + 2, B_OEMPTY = B_OFULL + 2, B_DRAIN = B_OEMPTY + 2,
-                       B_TURN = B_DRAIN + 1, B_PHALF = B_TURN + 2, NUM_BARS = B_PHALF + 2;
+                       B_TURN = B_DRAIN + 1, B_PHALF = B_TURN + 2, B_MERGE = B_PHALF + 2, NUM_BARS = B_MERGE + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alignment
+  // (m, l) of every row of both tile slots for the merge of key-split units
+  // (D = 64 only: at D = 128 the rings leave no room)
+  static constexpr uint32_t MRG_BYTES = (D == 64) ? 2u * BM * 8u : 0u;
+  static constexpr uint32_t OFF_MRG = OFF_MISC + 16;
+  static constexpr uint32_t SMEM_BYTES = OFF_MRG + MRG_BYTES + 1024;   // + slack for 1024-byte alignment
   // TMEM column of S_t and O_t
   __device__ static constexpr uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
   __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * D; }
@@ -88,6 +92,7 @@ struct Unit {
   int b, h;
   int row0[2];   // first query row of tile 0 / 1 (Nq: the tile does not exist)
   int n[2];      // K/V tiles visited by query tile 0 / 1
+  int k0[2];     // index of the first of them
 };
 
 __device__ __forceinline__ int kv_tiles_for(int q0, const PrefillParams& p) {
@@ -103,7 +108,7 @@ __device__ __forceinline__ int kv_tiles_for(int q0, const PrefillParams& p) {
 // (batch, head) with the heads of one KV group adjacent.  A block is two
 // 128-row tiles, or one when the problem has fewer two-tile blocks than the
 // GPU has SMs (then tile 1 does not exist and its warps idle).
-__device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p) {
+__device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p, bool ksplit) {
   Unit U;
   const int bh_count = p.B * p.Hq;
   const int qb_rev = u / bh_count;
@@ -111,6 +116,16 @@ __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p) {
   const int qb = p.nqb - 1 - qb_rev;
   U.b = bh / p.Hq;
   U.h = bh - U.b * p.Hq;
+  U.k0[0] = U.k0[1] = 0;
+  if (ksplit) {
+    // both slots take the same rows; slot 0 the first half of the key tiles
+    U.row0[0] = U.row0[1] = qb * BM;
+    const int n = kv_tiles_for(U.row0[0], p);
+    U.n[0] = (n + 1) / 2;
+    U.n[1] = n - U.n[0];
+    U.k0[1] = U.n[0];
+    return U;
+  }
   if (p.tiles_per_unit == 1) {
     U.row0[0] = qb * BM;
     U.row0[1] = p.Nq;
@@ -164,9 +179,99 @@ __device__ __forceinline__ void keep_pair_masks(uint32_t f, uint32_t& m01, uint3
   asm("prmt.b32 %0, %1, 0, 0xAABB;" : "=r"(m23) : "r"(f));
 }
 
+// Epilogue of a key-split unit: slots 0 and 1 hold the same rows' partial
+// states (O_t relative to the reference m_t, normaliser l_t) over the first
+// and second part of the key tiles.  With m = max(m_0, m_1) and
+// L = sum_t 2^(m_t - m) l_t, the row's output is sum_t 2^(m_t - m) O_t / L
+// (the same merge of partial softmax states as the split-KV combine), and
+// LSE = (m + log2 L) ln 2.  Each slot's warps write their rows' (m, l) to
+// shared memory, meet the other slot on an mbarrier, then merge and store
+// half of the columns (slot t: columns t D/2 .. (t+1) D/2 - 1), reading both
+// O tiles from TMEM (warps q and 4 + q reach the same TMEM lanes).  A second
+// meeting keeps both O tiles in TMEM until both halves are read.
+template <int D, bool DROP>
+__device__ __forceinline__ bool merge_epilogue(const PrefillParams& p, const Unit& U, int t, uint32_t quad,
+                                               uint32_t lane, int row_in_tile, float m_used, float l, uint32_t tm,
+                                               float2* mrg, uint32_t merge_bar, uint32_t& mph, const WaitCtx& wctx) {
+  using C = Cfg<D>;
+  mrg[t * BM + row_in_tile] = make_float2(m_used, l);
+  __syncwarp();
+  if (lane == 0) mbar_arrive(merge_bar);
+  if (!warp_wait(merge_bar, mph, wctx)) return false;
+  mph ^= 1u;
+  tc_fence_after();   // the other slot's O is complete (it waited for its commit before arriving)
+  const float2 oth = mrg[(t ^ 1) * BM + row_in_tile];
+  const float m0 = t ? oth.x : m_used, l0 = t ? oth.y : l;
+  const float m1 = t ? m_used : oth.x, l1 = t ? l : oth.y;
+  const float mm = fmaxf(m0, m1);
+  const float a0 = (m0 == -INFINITY) ? 0.f : ex2(m0 - mm);
+  const float a1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mm);
+  const float L = a0 * l0 + a1 * l1;
+  const float inv = (L > 0.f) ? (DROP ? p.drop_scale : 1.f) / L : 0.f;
+  const float f0 = a0 * inv, f1 = a1 * inv;
+  const int q0 = U.row0[0];
+  const long long ohead = U.b * p.o_sb + U.h * p.o_sh;
+  const bool bf = p.o_bf16 != nullptr;
+  const bool use0 = U.n[0] > 0, use1 = U.n[1] > 0;   // a slot with no key tile holds no O
+#pragma unroll 1
+  for (int hl = 0; hl < 2; ++hl) {
+    const int ra = static_cast<int>(quad * 32 + hl * 16 + (lane >> 2));   // rows ra and ra + 8 of the tile
+    const int src = hl * 16 + static_cast<int>(lane >> 2);
+    const float f0a = __shfl_sync(kFull, f0, src), f0b = __shfl_sync(kFull, f0, src + 8);
+    const float f1a = __shfl_sync(kFull, f1, src), f1b = __shfl_sync(kFull, f1, src + 8);
+    const bool la = q0 + ra < p.Nq, lb = q0 + ra + 8 < p.Nq;
+    const long long oa = ohead + (la ? q0 + ra : 0) * p.o_sr + 2 * (lane & 3);
+    const long long ob = ohead + (lb ? q0 + ra + 8 : 0) * p.o_sr + 2 * (lane & 3);
+    const uint32_t lanes16 = (quad * 32u + hl * 16u) << 16;
+#pragma unroll 1
+    for (int cc = 0; cc < D / 64; ++cc) {
+      const int col = t * (D / 2) + cc * 32;
+      uint32_t x0[16], x1[16];
+      if (use0) {
+        tmem_ld16x256b_x4(tm + lanes16 + C::col_o(0) + col, x0);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x0[i] = 0u;
+      }
+      if (use1) {
+        tmem_ld16x256b_x4(tm + lanes16 + C::col_o(1) + col, x1);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x1[i] = 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float y0 = __uint_as_float(x0[4 * k]) * f0a + __uint_as_float(x1[4 * k]) * f1a;
+        const float y1 = __uint_as_float(x0[4 * k + 1]) * f0a + __uint_as_float(x1[4 * k + 1]) * f1a;
+        const float z0 = __uint_as_float(x0[4 * k + 2]) * f0b + __uint_as_float(x1[4 * k + 2]) * f1b;
+        const float z1 = __uint_as_float(x0[4 * k + 3]) * f0b + __uint_as_float(x1[4 * k + 3]) * f1b;
+        const int c = col + 8 * k;
+        if (bf) {
+          if (la) *reinterpret_cast<uint32_t*>(p.o_bf16 + oa + c) = pack_bf16x2(y0, y1);
+          if (lb) *reinterpret_cast<uint32_t*>(p.o_bf16 + ob + c) = pack_bf16x2(z0, z1);
+        } else {
+          if (la) *reinterpret_cast<float2*>(p.o + oa + c) = make_float2(y0, y1);
+          if (lb) *reinterpret_cast<float2*>(p.o + ob + c) = make_float2(z0, z1);
+        }
+      }
+    }
+  }
+  const int row = q0 + row_in_tile;
+  if (t == 0 && row < p.Nq && p.lse != nullptr)
+    p.lse[static_cast<size_t>(U.b * p.Hq + U.h) * p.Nq + row] =
+        (L > 0.f) ? (mm + __log2f(L)) * 0.69314718055994531f : -INFINITY;
+  // both slots have read both O tiles before either is handed back
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(merge_bar);
+  if (!warp_wait(merge_bar, mph, wctx)) return false;
+  mph ^= 1u;
+  return true;
+}
+
 // SPLIT > 0: one exponential pair in every SPLIT on the FMA pipe (ex2_fma2),
-// the others on the SFU.
-template <int D, bool DROP, int SPLIT>
+// the others on the SFU.  KSPLIT: key-split units (D = 64 only).
+template <int D, bool DROP, int SPLIT, bool KSPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
@@ -181,6 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtx wctx{abort_flag, p.err};
 
   const uint32_t warp = warp_id(), lane = lane_id();
+  static_assert(!KSPLIT || C::MRG_BYTES > 0, "key-split units need the merge buffer");
+  constexpr bool ksplit = KSPLIT;
 
   if (threadIdx.x == 0) {
     *abort_flag = 0u;
@@ -204,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_DRAIN), 2);
     mbar_init(bar(C::B_TURN + 0), 1);
     mbar_init(bar(C::B_TURN + 1), 1);
+    if constexpr (KSPLIT) mbar_init(bar(C::B_MERGE), 8);   // the eight softmax warps
     fence_mbar_init();
   }
   if (warp == kMmaWarp0) {
@@ -238,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0;; ++it) {
         const int u = unit_at(it);
         if (u >= p.num_units) break;
-        const Unit U = decode_unit(u, p);
+        const Unit U = decode_unit(u, p, ksplit);
         bool ok = true;
         for (int t = 0; t < 2 && ok; ++t) {
           if (U.n[t] == 0) continue;
@@ -254,21 +362,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const int nmax = max(U.n[0], U.n[1]);
         const int kvh = U.h / group;
-        for (int j = 0; j < nmax && ok; ++j) {
-          if (!(ok = mbar_wait(bar(C::B_KEMPTY + ks), kph ^ 1u, wctx))) break;
-          mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::KV_BYTES);
-          note_fill(2 + ks, kph);
-          for (int kc = 0; kc < C::KCH; ++kc)
-            tma_load_4d(sK + ks * C::KV_BYTES + kc * C::CHUNK_KV, &tmK, bar(C::B_KFULL + ks), kc * 64,
-                        p.token_major ? kvh : j * BN, p.token_major ? j * BN : kvh, U.b, pol_kv);
-          if (++ks == C::KS) { ks = 0; kph ^= 1u; }
-          if (!(ok = mbar_wait(bar(C::B_VEMPTY + vs), vph ^ 1u, wctx))) break;
-          mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::KV_BYTES);
-          note_fill(2 + C::KS + vs, vph);
-          for (int kc = 0; kc < C::KCH; ++kc)
-            tma_load_4d(sV + vs * C::KV_BYTES + kc * C::CHUNK_KV, &tmV, bar(C::B_VFULL + vs), kc * 64,
-                        p.token_major ? kvh : j * BN, p.token_major ? j * BN : kvh, U.b, pol_kv);
-          if (++vs == C::VS) { vs = 0; vph ^= 1u; }
+        if constexpr (KSPLIT) {
+          // One ring position per step, or two for a key-split unit (slot 0's
+          // key tile, then slot 1's).  A slot with no key tile at a step gets
+          // its position completed by a plain arrive, so both MMA warps still
+          // walk every position in order.
+          const int lanes = ksplit ? 2 : 1;
+          for (int j = 0; j < nmax && ok; ++j) {
+            for (int tt = 0; tt < lanes; ++tt) {
+              if (!(ok = mbar_wait(bar(C::B_KEMPTY + ks), kph ^ 1u, wctx))) break;
+              note_fill(2 + ks, kph);
+              const int kt = U.k0[tt] + j;
+              if (lanes == 1 || j < U.n[tt]) {
+                mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::KV_BYTES);
+                for (int kc = 0; kc < C::KCH; ++kc)
+                  tma_load_4d(sK + ks * C::KV_BYTES + kc * C::CHUNK_KV, &tmK, bar(C::B_KFULL + ks), kc * 64,
+                              p.token_major ? kvh : kt * BN, p.token_major ? kt * BN : kvh, U.b, pol_kv);
+              } else {
+                mbar_arrive(bar(C::B_KFULL + ks));
+              }
+              if (++ks == C::KS) { ks = 0; kph ^= 1u; }
+            }
+            for (int tt = 0; tt < lanes && ok; ++tt) {
+              if (!(ok = mbar_wait(bar(C::B_VEMPTY + vs), vph ^ 1u, wctx))) break;
+              note_fill(2 + C::KS + vs, vph);
+              const int kt = U.k0[tt] + j;
+              if (lanes == 1 || j < U.n[tt]) {
+                mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::KV_BYTES);
+                for (int kc = 0; kc < C::KCH; ++kc)
+                  tma_load_4d(sV + vs * C::KV_BYTES + kc * C::CHUNK_KV, &tmV, bar(C::B_VFULL + vs), kc * 64,
+                              p.token_major ? kvh : kt * BN, p.token_major ? kt * BN : kvh, U.b, pol_kv);
+              } else {
+                mbar_arrive(bar(C::B_VFULL + vs));
+              }
+              if (++vs == C::VS) { vs = 0; vph ^= 1u; }
+            }
+          }
+        } else {
+          for (int j = 0; j < nmax && ok; ++j) {
+            if (!(ok = mbar_wait(bar(C::B_KEMPTY + ks), kph ^ 1u, wctx))) break;
+            mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::KV_BYTES);
+            note_fill(2 + ks, kph);
+            for (int kc = 0; kc < C::KCH; ++kc)
+              tma_load_4d(sK + ks * C::KV_BYTES + kc * C::CHUNK_KV, &tmK, bar(C::B_KFULL + ks), kc * 64,
+                          p.token_major ? kvh : j * BN, p.token_major ? j * BN : kvh, U.b, pol_kv);
+            if (++ks == C::KS) { ks = 0; kph ^= 1u; }
+            if (!(ok = mbar_wait(bar(C::B_VEMPTY + vs), vph ^ 1u, wctx))) break;
+            mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::KV_BYTES);
+            note_fill(2 + C::KS + vs, vph);
+            for (int kc = 0; kc < C::KCH; ++kc)
+              tma_load_4d(sV + vs * C::KV_BYTES + kc * C::CHUNK_KV, &tmV, bar(C::B_VFULL + vs), kc * 64,
+                          p.token_major ? kvh : j * BN, p.token_major ? j * BN : kvh, U.b, pol_kv);
+            if (++vs == C::VS) { vs = 0; vph ^= 1u; }
+          }
         }
         if (!ok) break;
       }
@@ -309,17 +455,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0;; ++it) {
         const int u = unit_at(it);
         if (u >= p.num_units) break;
-        const Unit U = decode_unit(u, p);
+        const Unit U = decode_unit(u, p, ksplit);
         const int n = t ? U.n[1] : U.n[0];
         const int nmax = max(U.n[0], U.n[1]);
+        // ring positions per step (two in a key-split unit: slot 0's, then
+        // slot 1's); both warps wait for and release every position, and
+        // each uses its own
+        const int lanes = ksplit ? 2 : 1;
+        const int own = ksplit ? t : 0;
         bool o_waited = false;
         bool ok = true;
         for (int j = 0; j <= nmax && ok; ++j) {
           const bool do_pv = j >= 1 && j - 1 < n;
           const bool do_s = j < n;
           // every wait of this step first, then the turn
-          if (j >= 1 && !(ok = warp_wait(bar(C::B_VFULL + vs), vph, wctx))) break;
-          if (j < nmax && !(ok = warp_wait(bar(C::B_KFULL + ks), kph, wctx))) break;
+          int vs_own = vs, ks_own = ks;
+          if constexpr (KSPLIT) {
+            if (j >= 1)
+              for (int o = 0; o < lanes && ok; ++o)
+                ok = warp_wait(bar(C::B_VFULL + (vs + o) % C::VS), vph ^ ((vs + o) >= C::VS ? 1u : 0u), wctx);
+            if (!ok) break;
+            if (j < nmax)
+              for (int o = 0; o < lanes && ok; ++o)
+                ok = warp_wait(bar(C::B_KFULL + (ks + o) % C::KS), kph ^ ((ks + o) >= C::KS ? 1u : 0u), wctx);
+            if (!ok) break;
+            vs_own = (vs + own) % C::VS;
+            ks_own = (ks + own) % C::KS;
+          } else {
+            if (j >= 1 && !(ok = warp_wait(bar(C::B_VFULL + vs), vph, wctx))) break;
+            if (j < nmax && !(ok = warp_wait(bar(C::B_KFULL + ks), kph, wctx))) break;
+          }
           if (do_pv) {
             if (!o_waited) {
               if (!(ok = warp_wait(bar(C::B_OEMPTY + t), oeph ^ 1u, wctx))) break;
@@ -341,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (do_pv) {
             // O_t += P_t(j-1) V_{j-1}; P read from TMEM over S_t
             // keys 0..63 as soon as their P is in TMEM, keys 64..127 after
-            const uint64_t vd = v_desc0 + ((vs * C::KV_BYTES) >> 4);
+            const uint64_t vd = v_desc0 + ((vs_own * C::KV_BYTES) >> 4);
             {
               uint32_t a[4];
               uint64_t b[4];
@@ -362,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (do_s) {
             // S_t = Q_t K_j^T, one 64-feature chunk (four MMAs) per elect
-            const uint64_t kd = k_desc0 + ((ks * C::KV_BYTES) >> 4);
+            const uint64_t kd = k_desc0 + ((ks_own * C::KV_BYTES) >> 4);
 #pragma unroll
             for (int kc = 0; kc < C::KCH; ++kc) {
               uint64_t a[4], b[4];
@@ -380,13 +545,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j == n - 1) mma_commit_warp(bar(C::B_QEMPTY + t));
           }
           if (j == n && n > 0) mma_commit_warp(bar(C::B_OFULL + t));
-          if (j < nmax) {
-            mma_commit_warp(bar(C::B_KEMPTY + ks));
-            if (++ks == C::KS) { ks = 0; kph ^= 1u; }
-          }
-          if (j >= 1) {
-            mma_commit_warp(bar(C::B_VEMPTY + vs));
-            if (++vs == C::VS) { vs = 0; vph ^= 1u; }
+          if constexpr (KSPLIT) {
+            if (j < nmax)
+              for (int o = 0; o < lanes; ++o) {
+                mma_commit_warp(bar(C::B_KEMPTY + ks));
+                if (++ks == C::KS) { ks = 0; kph ^= 1u; }
+              }
+            if (j >= 1)
+              for (int o = 0; o < lanes; ++o) {
+                mma_commit_warp(bar(C::B_VEMPTY + vs));
+                if (++vs == C::VS) { vs = 0; vph ^= 1u; }
+              }
+          } else {
+            if (j < nmax) {
+              mma_commit_warp(bar(C::B_KEMPTY + ks));
+              if (++ks == C::KS) { ks = 0; kph ^= 1u; }
+            }
+            if (j >= 1) {
+              mma_commit_warp(bar(C::B_VEMPTY + vs));
+              if (++vs == C::VS) { vs = 0; vph ^= 1u; }
+            }
           }
         }
         if (!ok) break;
@@ -416,14 +594,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     const uint32_t cdrop = (256u - p.drop_t) * 0x00800080u;
     const int delta = p.Nkv - p.Nq;
-    uint32_t sph = 0, ofph = 0;
+    uint32_t sph = 0, ofph = 0, mph = 0;
     for (int it = 0;; ++it) {
       const int u = unit_at(it);
       if (u >= p.num_units) break;
-      const Unit U = decode_unit(u, p);
+      const Unit U = decode_unit(u, p, ksplit);
       const int n = t ? U.n[1] : U.n[0];
       const int q0 = U.row0[t];
       const int row = q0 + row_in_tile;
+      const int kt0 = KSPLIT ? (t ? U.k0[1] : U.k0[0]) : 0;   // first key tile of this slot
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
@@ -434,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (DROP) {
 #pragma unroll
           for (int g = 0; g < BN / 16; ++g) {
-            const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>(j * (BN / 16) + g),
+            const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>((kt0 + j) * (BN / 16) + g),
                                                      static_cast<uint32_t>(row), static_cast<uint32_t>(U.h),
                                                      static_cast<uint32_t>(U.b)),
                                           p.seed_lo, p.seed_hi);
@@ -447,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = warp_wait(bar(C::B_SFULL + t), sph, wctx))) break;
         sph ^= 1u;
         tc_fence_after();
-        const int key0 = j * BN;
+        const int key0 = (kt0 + j) * BN;
         const bool need_mask = (key0 + BN > p.Nkv) || (p.causal && key0 + BN - 1 > q0 + delta);
         const int key_lim = p.causal ? min(row + delta, p.Nkv - 1) : p.Nkv - 1;   // last visible key
         // The whole 128-column S row in registers: one TMEM load per tile.
@@ -551,6 +730,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       ofph ^= 1u;
       tc_fence_after();
       const bool live = row < p.Nq;
+      if constexpr (KSPLIT) {
+        if (ksplit) {
+          if (!(ok = merge_epilogue<D, DROP>(p, U, t, quad, lane, row_in_tile, m_used, l, tm,
+                                             reinterpret_cast<float2*>(smem + C::OFF_MRG), bar(C::B_MERGE), mph,
+                                             wctx)))
+            break;
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + t));
+          continue;
+        }
+      }
       const float inv_l = (l > 0.f) ? (DROP ? p.drop_scale : 1.f) / l : 0.f;
       // O leaves TMEM in the 16x256b shape: each store instruction of the
       // warp then writes 8 rows x 32 contiguous bytes (whole sectors),
@@ -608,11 +799,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool DROP, int SPLIT>
+template <int D, bool DROP, int SPLIT, bool KSPLIT = false>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                      int num_sms, cudaStream_t stream) {
   using C = Cfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, DROP, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, DROP, SPLIT, KSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM_BYTES));
   if (e != cudaSuccess) return e;
   const int grid = min(p.num_units, num_sms);
@@ -620,9 +811,9 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
   // The register split needs the kernel to be launched with enough registers;
   // otherwise setmaxnreg.inc could never be served, so refuse to launch.
   cudaFuncAttributes fa;
-  if ((e = cudaFuncGetAttributes(&fa, prefill_kernel<D, DROP, SPLIT>)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&fa, prefill_kernel<D, DROP, SPLIT, KSPLIT>)) != cudaSuccess) return e;
   if (((fa.numRegs + 7) / 8) * 8 < kRegsNeededAtLaunch) return cudaErrorInvalidConfiguration;
-  prefill_kernel<D, DROP, SPLIT><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  prefill_kernel<D, DROP, SPLIT, KSPLIT><<<grid, kThreads, C::SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -631,6 +822,16 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 cudaError_t launch_prefill(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int num_sms, cudaStream_t stream) {
   const bool drop = p.drop_t != 0u;
+  if (d == 64 && p.kv_split) {
+    if (drop) return launch_d<64, true, 0, true>(tq, tk, tv, p, num_sms, stream);
+    switch (p.exp2_split) {
+      case 0: return launch_d<64, false, 0, true>(tq, tk, tv, p, num_sms, stream);
+      case 4: return launch_d<64, false, 4, true>(tq, tk, tv, p, num_sms, stream);
+      case 8: return launch_d<64, false, 8, true>(tq, tk, tv, p, num_sms, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (p.kv_split) return cudaErrorInvalidValue;   // key-split units exist at d = 64 only
   if (drop) {
     if (d == 64) return launch_d<64, true, 0>(tq, tk, tv, p, num_sms, stream);
     if (d == 128) return launch_d<128, true, 0>(tq, tk, tv, p, num_sms, stream);

@@ -96,6 +96,33 @@ SMALL = [
 
 LATENT = [w for w in SMALL if w.d_qk == 576]
 
+# Problems under one wave at d = 64 run key-split units: both tile slots take
+# one query tile and share out its key tiles, and their partial states are
+# merged in the epilogue.  Even and odd key-tile counts, large logits (both
+# parts rescale), and causal rows that see no key.
+KSPLIT = [
+    W("ksplit_even_d64", B=1, Hq=4, Hkv=2, Nq=512, Nkv=1024, d_qk=64, d_v=64, causal=False, scale=0.125),
+    W("ksplit_causal_bigq_d64", B=2, Hq=3, Hkv=1, Nq=640, Nkv=640, d_qk=64, d_v=64, causal=True, scale=0.125,
+      q_factor=8.0),
+    W("ksplit_causal_nq_gt_nkv_d64", B=1, Hq=2, Hkv=1, Nq=300, Nkv=129, d_qk=64, d_v=64, causal=True, scale=0.125),
+    W("ksplit_two_key_tiles_d64", B=3, Hq=2, Hkv=2, Nq=129, Nkv=256, d_qk=64, d_v=64, causal=False, scale=0.125),
+]
+D64_UNDER_ONE_WAVE = [w for w in SMALL + KSPLIT
+                      if w.d_qk == 64 and w.B * w.Hq * ((w.Nq + 255) // 256) < 152]
+
+
+@pytest.mark.parametrize("wl", KSPLIT, ids=lambda w: w.name)
+def test_key_split_units_full_parity(wl):
+    full_case(wl)
+
+
+@pytest.mark.parametrize("wl", D64_UNDER_ONE_WAVE, ids=lambda w: w.name)
+def test_single_tile_units_full_parity(wl, monkeypatch):
+    """ATTN_PREFILL_KVSPLIT=0: the same problems with one tile per unit and
+    the second slot idle meet the same bar."""
+    monkeypatch.setenv("ATTN_PREFILL_KVSPLIT", "0")
+    full_case(wl)
+
 
 @pytest.mark.parametrize("wl", LATENT, ids=lambda w: w.name)
 def test_latent_one_cta_kernel_full_parity(wl, monkeypatch):
