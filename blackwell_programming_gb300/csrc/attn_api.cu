@@ -21,6 +21,7 @@
 #include <cudaTypedefs.h>
 
 #include "gbattn.h"
+#include "philox.cuh"
 #include "gbgemm.h"
 #include "gblayer.h"
 #include "internal.h"
@@ -464,6 +465,7 @@ int run_prefill(const void* q, const void* k, const void* v, float* o32, uint16_
   p.scale_log2 = scale_log2;
   p.seed_lo = static_cast<uint32_t>(drop.seed & 0xFFFFFFFFull);
   p.seed_hi = static_cast<uint32_t>(drop.seed >> 32);
+  philox_round_keys(p.seed_lo, p.seed_hi, p.round_keys);
   p.drop_t = drop.t;
   p.drop_scale = static_cast<float>(256.0 / (256.0 - static_cast<double>(drop.t)));
   // Two 128-row tiles per unit (they ping-pong on the tensor core); one when

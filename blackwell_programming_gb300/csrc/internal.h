@@ -30,6 +30,10 @@ struct PrefillParams {
   // by drop_scale = 256 / (256 - drop_t) in the epilogue.
   uint32_t seed_lo, seed_hi, drop_t;
   float drop_scale;
+  // The generator's key for each of its ten rounds, (k0, k1) of round r at
+  // [2r], [2r + 1]: the key schedule is the same for every call, so the
+  // kernel reads it from its parameters instead of advancing the key.
+  uint32_t round_keys[20];
   // Exponentials on the FMA pipe: one pair in every exp2_split (0, 4 or 8;
   // 0 = all on the SFU), dropout-free kernels only.
   int exp2_split;

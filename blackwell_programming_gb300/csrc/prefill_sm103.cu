@@ -613,10 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (DROP) {
 #pragma unroll
           for (int g = 0; g < BN / 16; ++g) {
-            const uint4 r = philox4x32_10(make_uint4(static_cast<uint32_t>((kt0 + j) * (BN / 16) + g),
-                                                     static_cast<uint32_t>(row), static_cast<uint32_t>(U.h),
-                                                     static_cast<uint32_t>(U.b)),
-                                          p.seed_lo, p.seed_hi);
+            const uint4 r = philox4x32_10_rk(make_uint4(static_cast<uint32_t>((kt0 + j) * (BN / 16) + g),
+                                                        static_cast<uint32_t>(row), static_cast<uint32_t>(U.h),
+                                                        static_cast<uint32_t>(U.b)),
+                                             p.round_keys);
             // two words' flags per register: the first word's on bit 7 of
             // each byte, the second's on bit 6
             rw[2 * g] = keep_flags2(keep_flags(r.x, cdrop), keep_flags(r.y, cdrop));
