@@ -30,6 +30,9 @@
 //    thread owns a whole row: max, exp2 and sum stay in-thread.  They also
 //    rescale O (only when the running max grew by more than 2^8, which keeps
 //    the result exact) and run the epilogue: O / l and LSE to global memory.
+//  * Problems under one wave at D = 64 run key-split units (KSPLIT): both
+//    query tiles are the same rows over two halves of the key tiles, and the
+//    epilogue merges the two partial softmax states.
 //
 // TMEM columns: S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D).
 #include <cmath>
@@ -107,7 +110,9 @@ __device__ __forceinline__ int kv_tiles_for(int q0, const PrefillParams& p) {
 // Unit u: query-block index descending (longest causal work first), then
 // (batch, head) with the heads of one KV group adjacent.  A block is two
 // 128-row tiles, or one when the problem has fewer two-tile blocks than the
-// GPU has SMs (then tile 1 does not exist and its warps idle).
+// GPU has SMs: then tile 1 does not exist and its warps idle, or, in a
+// key-split kernel, both tile slots take the one tile and share out its key
+// tiles (slot 0 the first ceil(n / 2), slot 1 the rest).
 __device__ __forceinline__ Unit decode_unit(int u, const PrefillParams& p, bool ksplit) {
   Unit U;
   const int bh_count = p.B * p.Hq;
@@ -363,17 +368,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nmax = max(U.n[0], U.n[1]);
         const int kvh = U.h / group;
         if constexpr (KSPLIT) {
-          // One ring position per step, or two for a key-split unit (slot 0's
-          // key tile, then slot 1's).  A slot with no key tile at a step gets
-          // its position completed by a plain arrive, so both MMA warps still
-          // walk every position in order.
-          const int lanes = ksplit ? 2 : 1;
+          // Two ring positions per step: slot 0's key tile, then slot 1's.
+          // A slot with no key tile at a step gets its position completed by
+          // a plain arrive, so both MMA warps still walk every position in
+          // order.
           for (int j = 0; j < nmax && ok; ++j) {
-            for (int tt = 0; tt < lanes; ++tt) {
+            for (int tt = 0; tt < 2; ++tt) {
               if (!(ok = mbar_wait(bar(C::B_KEMPTY + ks), kph ^ 1u, wctx))) break;
               note_fill(2 + ks, kph);
               const int kt = U.k0[tt] + j;
-              if (lanes == 1 || j < U.n[tt]) {
+              if (j < U.n[tt]) {
                 mbar_arrive_expect_tx(bar(C::B_KFULL + ks), C::KV_BYTES);
                 for (int kc = 0; kc < C::KCH; ++kc)
                   tma_load_4d(sK + ks * C::KV_BYTES + kc * C::CHUNK_KV, &tmK, bar(C::B_KFULL + ks), kc * 64,
@@ -383,11 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               if (++ks == C::KS) { ks = 0; kph ^= 1u; }
             }
-            for (int tt = 0; tt < lanes && ok; ++tt) {
+            for (int tt = 0; tt < 2 && ok; ++tt) {
               if (!(ok = mbar_wait(bar(C::B_VEMPTY + vs), vph ^ 1u, wctx))) break;
               note_fill(2 + C::KS + vs, vph);
               const int kt = U.k0[tt] + j;
-              if (lanes == 1 || j < U.n[tt]) {
+              if (j < U.n[tt]) {
                 mbar_arrive_expect_tx(bar(C::B_VFULL + vs), C::KV_BYTES);
                 for (int kc = 0; kc < C::KCH; ++kc)
                   tma_load_4d(sV + vs * C::KV_BYTES + kc * C::CHUNK_KV, &tmV, bar(C::B_VFULL + vs), kc * 64,
