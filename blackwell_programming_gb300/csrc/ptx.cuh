@@ -438,18 +438,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 // 8k + 2(i mod 4) and 8k + 2(i mod 4) + 1 of lane i/4 (registers 4k, 4k+1)
 // and of lane i/4 + 8 (registers 4k+2, 4k+3).  `taddr`'s lane must be the
 // first of a 16-lane group inside the warp's own quarter of TMEM.
-// The same load without the wait: the registers are valid only after
-// tmem_ld_wait(), so nothing may read them before it.
-__device__ __forceinline__ void tmem_ld16x256b_x4_async(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
 // 16 lanes x 256 bits, 4 repeats (32 columns), then wait: thread i gets rows
 // base + i/4 (r[4k], r[4k+1]) and base + 8 + i/4 (r[4k+2], r[4k+3]) at
 // columns 8k + 2(i mod 4) and the next one.
